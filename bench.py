@@ -1,0 +1,420 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA / HCA hot path on B300.
+
+Default workload: CSA decode at 1M context -- 32 sequences, one query each,
+each against its own 262,144-entry compressed cache (E4M3 indexer keys with
+per-row fp32 scales, BF16 K_c / V_c), 64 x 128 indexer, top-k 1024, 64 x 128
+attention.  One step = Lightning-Indexer scores + top-k + sparse attention
+for the 32 queries, through the C ABI.  Inputs (5.2 GB) stay resident in HBM
+and exceed L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead (the reference arm).  ``--config NAME`` times another named workload
+(per-call CUDA-event times; for measurements, not the headline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA queries/s at 1M ctx (idx+topk+attn); HBM GB/s & TC util vs peak"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default="csa_decode_b32_ctx1m_e4m3")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--batch", type=int, default=0, help="override the decode batch (profiling runs)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current source of that kernel (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[kernel]
+        src = open(os.path.join(ROOT, "long_context_compressed_18_b300", "csrc", e["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != e["source_sha256"] or e["workload"] != workload:
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _gpu_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return "0"
+
+
+# ---------------------------------------------------------------------------
+def _decode_shape(args, rank):
+    from long_context_compressed_18_b300 import configs
+    s = configs.CSA_DECODE_1M
+    kw = dict(s.__dict__)
+    kw["seed"] = s.seed + 7919 * rank          # each rank: its own 32 sequences
+    if args.batch:
+        kw["B"] = args.batch
+    return configs.Shape(**kw)
+
+
+def _oracle_queries(s, x, bs, entry_stride=1):
+    """The oracle's idx + top-k + attention for sequences ``bs`` (host copies),
+    scoring every ``entry_stride``-th entry.  Returns seconds."""
+    import numpy as np
+    import oracle
+    t_total = 0.0
+    for b in bs:
+        iq, iqs = x["idx_q"][b:b + 1].cpu(), x["idx_q_scale"][b:b + 1].cpu()
+        ik = x["idx_k_c"][b:b + 1, ::entry_stride].cpu().contiguous()
+        iks = x["idx_k_c_scale"][b:b + 1, ::entry_stride].cpu().contiguous()
+        kc = x["k_c"][b:b + 1].cpu()
+        vc = x["v_c"][b:b + 1].cpu()
+        q = x["q"][b:b + 1].cpu()
+        Nc = ik.shape[1]
+        t0 = time.perf_counter()
+        _, _, sel = oracle.csa_index_topk(iq, iqs, "e4m3", ik, iks, "e4m3", Nc * s.m - 1, s.m, s.k)
+        oracle.attention(q, kc, vc, 1.0 / math.sqrt(s.d), oracle.SPARSE, idx=sel[None] * entry_stride)
+        t_total += time.perf_counter() - t0
+    return t_total
+
+
+def run_decode(args, torch, dist, rank, world):
+    from long_context_compressed_18_b300 import inputs, lib
+    import oracle  # noqa: F401  (cpu_baseline leg only)
+
+    dev = torch.cuda.current_device()
+    s = _decode_shape(args, rank)
+    B, Nc, k, HI, dI, H, d = s.B, s.N_c, s.k, s.H_I, s.d_I, s.H, s.d
+    x = inputs.make_inputs(s, device="cuda")
+    scores = torch.empty(B, 1, Nc, dtype=torch.float32, device="cuda")
+    topk = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, 1, H, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, 1, H, dtype=torch.float32, device="cuda")
+    ws_t_b = lib.csa_topk_select_workspace_size(B, 1, Nc, k)
+    ws_a_b = lib.csa_sparse_attn_workspace_size(B, 1, H, d, k)
+    ws_t = lib.empty_workspace(ws_t_b)
+    ws_a = lib.empty_workspace(ws_a_b)
+    tau = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        lib.csa_index_scores(B, 1, s.q_pos0, s.m, Nc, HI, dI, x["idx_q"], lib.E4M3, x["idx_q_scale"],
+                             x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], scores)
+        if ev:
+            ev[1].record(stream)
+        lib.csa_topk_select(B, 1, s.q_pos0, s.m, Nc, k, scores, topk, ws_t, ws_t_b)
+        if ev:
+            ev[2].record(stream)
+        lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, x["q"], x["k_c"], x["v_c"], lib.BF16, topk, out, lse,
+                            ws_a, ws_a_b)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lib.csa_device_status()
+
+    # ---- timed region: K steps, per-call events ----
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(_gpu_id(torch, dev)) as clk:
+        t_start.record(stream)
+        for i in range(K):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    lib.csa_device_status()
+    per = {"indexer": [], "topk": [], "sparse_attn": []}
+    for e in evs:
+        per["indexer"].append(e[0].elapsed_time(e[1]))
+        per["topk"].append(e[1].elapsed_time(e[2]))
+        per["sparse_attn"].append(e[2].elapsed_time(e[3]))
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- e2e: same step through the C ABI, queries from pinned host memory ----
+    e2e = None
+    if not args.no_e2e:
+        h_in = {kk: x[kk].cpu().pin_memory() for kk in ("q", "idx_q", "idx_q_scale")}
+        d_in = {kk: torch.empty_like(x[kk]) for kk in h_in}
+        h_out = {"out": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                 "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory(),
+                 "topk": torch.empty(topk.shape, dtype=topk.dtype).pin_memory()}
+        bi = sum(t.numel() * t.element_size() for t in h_in.values())
+        bo = sum(t.numel() * t.element_size() for t in h_out.values())
+
+        def e2e_step():
+            for kk in h_in:
+                d_in[kk].copy_(h_in[kk], non_blocking=True)
+            lib.csa_index_scores(B, 1, s.q_pos0, s.m, Nc, HI, dI, d_in["idx_q"], lib.E4M3, d_in["idx_q_scale"],
+                                 x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], scores)
+            lib.csa_topk_select(B, 1, s.q_pos0, s.m, Nc, k, scores, topk, ws_t, ws_t_b)
+            lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, d_in["q"], x["k_c"], x["v_c"], lib.BF16, topk, out, lse,
+                                ws_a, ws_a_b)
+            h_out["out"].copy_(out, non_blocking=True)
+            h_out["lse"].copy_(lse, non_blocking=True)
+            h_out["topk"].copy_(topk, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        K2 = max(10, K // 4)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        a.record(stream)
+        for _ in range(K2):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        ms2 = a.elapsed_time(b_)
+        if dist:
+            t = torch.tensor([ms2], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms2 = float(t.item())
+        e2e = {"value": world * B * K2 / (ms2 / 1e3), "unit": "queries/s", "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo,
+               "note": "per-step H2D of the 32 queries (q, indexer q + scales) and D2H of out, lse, top-k; "
+                       "the compressed caches are resident decode state"}
+
+    # ---- roofline of the dominant call ----
+    peaks, peak_src = _peaks()
+    avg = {kk: statistics.mean(v) for kk, v in per.items()}
+    dom = max(avg, key=avg.get)
+    alg = {  # algorithmic bytes per launch
+        "indexer": B * (Nc * (dI + 4) + HI * (dI + 4)),
+        "topk": B * Nc * 4,
+        "sparse_attn": B * (k * d * 2 * 2 + H * d * 2 * 2 + k * 4 + H * 4),
+    }
+    achieved = alg[dom] / (avg[dom] / 1e3) / 1e9
+    traffic = _traffic({"indexer": "indexer_tc_kernel", "topk": "topk_kernel", "sparse_attn": "attn_simt_kernel"}[dom],
+                       s.name)
+    roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "peak_source": peak_src, "algorithmic_bytes_per_launch": alg[dom],
+            "avg_launch_ms": round(avg[dom], 5)}
+
+    # ---- cpu baseline: the oracle on a bounded sample (rank 0, N = 1) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t1 = _oracle_queries(s, x, [0])
+        nq = int(max(1, min(8, round(15.0 / max(t1, 1e-3)))))
+        bs = [(7 * i) % B for i in range(nq)]
+        tt = _oracle_queries(s, x, bs)
+        cpu = {"value": nq / tt, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{nq} of the 32 decode queries (full 262,144-entry caches), {tt:.1f} s"}
+
+    launches_per_step = 1 + (2 if lib.csa_topk_select_workspace_size(B, 1, Nc, k) else 1) + \
+        (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
+    res = {
+        "metric": METRIC, "value": world * B * K / (ms / 1e3), "unit": "queries/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (indexer) / bf16 (attention)",
+        "data": "synthetic",
+        "config": {"workload": s.name, "batch_per_gpu": B, "ctx_tokens": s.n, "compressed_entries": Nc,
+                   "indexer": f"{HI}x{dI} e4m3", "top_k": k, "attention": f"{H}x{d} bf16",
+                   "l2": "inputs (5.2 GB per GPU) exceed L2; no flush",
+                   "parallelism": f"dp{world} (independent sequences per GPU)"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+        "per_call_ms": {kk: round(v, 5) for kk, v in avg.items()},
+    }
+    return res
+
+
+# ---------------------------------------------------------------------------
+def run_config(args, torch, name):
+    """Per-call timing of another named workload (one rank)."""
+    from long_context_compressed_18_b300 import configs, inputs, pipeline
+    layers = configs.STACK_LAYERS if name == "stack" else (configs.NAMED[name],)
+    ws = pipeline.Workspace()
+    xs = [inputs.make_inputs(s, device="cuda") for s in layers]
+    stream = torch.cuda.current_stream()
+    for _ in range(max(1, args.warmup)):
+        for s, x in zip(layers, xs):
+            pipeline.run_layer(x, s, ws)
+    torch.cuda.synchronize()
+    res = {}
+    with ClockSampler(_gpu_id(torch, torch.cuda.current_device())) as clk:
+        for s, x in zip(layers, xs):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                pipeline.run_layer(x, s, ws)
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[s.name] = a.elapsed_time(b) / args.steps
+    tot = sum(res.values())
+    n_q = sum(s.B * s.n_q for s in layers)
+    return {"metric": "queries/s (prefill)", "value": n_q / (tot / 1e3), "unit": "queries/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot, "higher_is_better": True,
+            "config": {"workload": name}, "per_layer_ms": res, "clocks": clk.summary(), "data": "synthetic"}
+
+
+def run_reference(args, torch, rank, world):
+    """Reference arm: the CPU oracle, on the host cores, on the same workload
+    and metric.  Each step is a bounded sample: one decode query whose cache
+    is strided by R (scoring 262,144 / R entries); the value is scaled by 1/R."""
+    if rank != 0:
+        return None
+    import oracle
+    from long_context_compressed_18_b300 import inputs
+    s = _decode_shape(args, 0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = inputs.make_inputs(s, device=dev, batches=list(range(4)))
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    t_full = _oracle_queries(s, x, [0], entry_stride=16) * 16
+    R = 1
+    while t_full / R > budget and R < 4096:
+        R *= 2
+    for i in range(args.warmup):
+        _oracle_queries(s, x, [i % 4], entry_stride=R)
+    tt = 0.0
+    for i in range(args.steps):
+        tt += _oracle_queries(s, x, [i % 4], entry_stride=R)
+    q_per_s = args.steps / R / tt
+    return {"impl": "reference", "metric": METRIC, "value": q_per_s, "unit": "queries/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": s.name},
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "value": q_per_s, "unit": "queries/s",
+                             "sample": f"one query per step over every {R}-th of its 262,144 entries, scaled by 1/{R}"},
+            "e2e": {"value": q_per_s, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = _args()
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        # rank 0 alone runs the oracle; the other ranks exit without work
+        res = run_reference(args, torch, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    if args.config == "csa_decode_b32_ctx1m_e4m3":
+        res = run_decode(args, torch, dist, rank, world)
+    else:
+        res = run_config(args, torch, args.config)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,449 @@
+// C ABI of the library (declared in include/csa.h): argument checks,
+// workspace planning, TMA descriptor encoding and kernel launches on the
+// caller's stream.  No device memory is allocated here.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/csa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+__device__ unsigned int g_status = 0;
+}
+
+using namespace csa;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+csa_status_t fail(csa_status_t st, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+csa_status_t cuda_status(cudaError_t e, const char* what)
+{
+    if (e == cudaSuccess) return CSA_OK;
+    return fail(CSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms()
+{
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D row-major [rows, inner] tensor, 128-byte swizzled boxes of
+// [box_rows, box_inner] (box_inner * element size = 128 bytes).
+csa_status_t make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
+                      uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(CSA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(CSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return CSA_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool tc_indexer_shape(int H_I, int d_I) { return H_I == 64 && d_I == 128; }
+
+csa_status_t check_index_dtypes(csa_dtype_t q_dtype, csa_dtype_t k_dtype, int H_I, int d_I)
+{
+    const bool f32 = q_dtype == CSA_F32 && k_dtype == CSA_F32;
+    const bool bf16 = q_dtype == CSA_BF16 && k_dtype == CSA_BF16;
+    const bool fp8 = q_dtype == CSA_E4M3 && (k_dtype == CSA_E4M3 || k_dtype == CSA_E2M1);
+    if (!f32 && !bf16 && !fp8)
+        return fail(CSA_ERR_UNSUPPORTED, "indexer precision pair (q=%d, k=%d) not supported", q_dtype, k_dtype);
+    if (!f32 && !tc_indexer_shape(H_I, d_I))
+        return fail(CSA_ERR_UNSUPPORTED, "tensor-core indexer needs H_I=64, d_I=128 (got %d, %d)", H_I, d_I);
+    if (f32 && (H_I < 1 || d_I < 1 || (size_t)(H_I * d_I + H_I) * 4 > 200 * 1024))
+        return fail(CSA_ERR_UNSUPPORTED, "fp32 indexer shape H_I=%d d_I=%d", H_I, d_I);
+    return CSA_OK;
+}
+
+// Workspace of the index-scores stage: widened E4M3 keys + row scales for E2M1.
+size_t scores_ws_bytes(int B, int N_c, int d_I, csa_dtype_t k_dtype)
+{
+    if (k_dtype != CSA_E2M1) return 0;
+    return align_up((size_t)B * N_c * d_I, 256) + align_up((size_t)B * N_c * 4, 256);
+}
+
+// Queries per chunk of csa_index_topk: bounded score buffer (multiple of 4).
+int index_chunk_rows(int B, int n_q, int N_c)
+{
+    const size_t budget = 256ull << 20;
+    size_t per_row = (size_t)B * (size_t)(N_c > 0 ? N_c : 1) * 4;
+    long long rows = (long long)(budget / per_row);
+    if (rows < 4) rows = 4;
+    rows &= ~3ll;
+    if (rows >= n_q) rows = n_q;
+    return (int)(rows > 0 ? rows : 1);
+}
+
+// Split-KV plan of the attention kernels.  Decode-shaped calls (few queries
+// per sequence) split each query's key set into slices of 128 so that one step
+// fills the GPU.  The plan depends only on the per-sequence shape, never on
+// the batch size, so a sequence's result is bitwise the same at any batch
+// position.
+int attn_splits(int n_q, long long set_len)
+{
+    if (n_q > 16 || set_len <= 128) return 1;
+    long long s = (set_len + 127) / 128;
+    return (int)(s > 64 ? 64 : s);
+}
+
+csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos0, int m, int N_c, int H_I,
+                        int d_I, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
+                        csa_dtype_t k_dtype, const void* k_scale, float* scores, void* ws, cudaStream_t s)
+{
+    if (q_dtype == CSA_F32) {
+        return cuda_status(launch_indexer_f32(reinterpret_cast<const float*>(q_idx), q_scale,
+                                              reinterpret_cast<const float*>(k_idx),
+                                              reinterpret_cast<const float*>(k_scale), scores, B, n_q, i_start,
+                                              n_q_rows, q_pos0, m, N_c, H_I, d_I, s),
+                           "indexer_f32 launch");
+    }
+    const bool fp8 = q_dtype == CSA_E4M3;
+    const void* keys = k_idx;
+    const float* ksc = reinterpret_cast<const float*>(k_scale);
+    if (k_dtype == CSA_E2M1) {
+        uint8_t* x8 = reinterpret_cast<uint8_t*>(ws);
+        float* S = reinterpret_cast<float*>(x8 + align_up((size_t)B * N_c * d_I, 256));
+        csa_status_t st = cuda_status(
+            launch_fp4_to_e4m3(reinterpret_cast<const uint8_t*>(k_idx), reinterpret_cast<const uint8_t*>(k_scale),
+                               x8, S, (long long)B * N_c, d_I, s),
+            "fp4_to_e4m3 launch");
+        if (st != CSA_OK) return st;
+        keys = x8;
+        ksc = S;
+    }
+    const int T = indexer_group_tokens(n_q_rows);
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t elem = fp8 ? 1 : 2;
+    const uint32_t box_inner = 128 / elem;
+    CUtensorMap tq, tk;
+    csa_status_t st = make_map(&tq, q_idx, dt, (uint64_t)d_I, (uint64_t)B * n_q * H_I, (uint64_t)d_I * elem, box_inner,
+                               (uint32_t)indexer_box_rows(T));
+    if (st != CSA_OK) return st;
+    st = make_map(&tk, keys, dt, (uint64_t)d_I, (uint64_t)B * N_c, (uint64_t)d_I * elem, box_inner, 128);
+    if (st != CSA_OK) return st;
+    return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, ksc, scores, B, n_q, i_start, n_q_rows, q_pos0, m,
+                                         N_c, num_sms(), s),
+                       "indexer_tc launch");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// attention
+// ---------------------------------------------------------------------------
+static csa_status_t check_attn(int B, int n_q, int H, int d, long long N_kv, const void* q, const void* k,
+                               const void* v, csa_dtype_t dtype, const void* out, const float* lse)
+{
+    if (B < 0 || n_q < 0 || N_kv < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes");
+    if (dtype != CSA_F32 && dtype != CSA_BF16) return fail(CSA_ERR_UNSUPPORTED, "attention dtype must be F32 or BF16");
+    if (!attn_simt_supported(H, d)) return fail(CSA_ERR_UNSUPPORTED, "attention needs H in {8,16,32,64,128}, d in {64,128}");
+    if ((long long)B * n_q == 0) return CSA_OK;
+    if (!q || !out || (N_kv > 0 && (!k || !v))) return fail(CSA_ERR_INVALID_ARG, "NULL tensor");
+    if (!aligned16(q) || !aligned16(out) || (k && !aligned16(k)) || (v && !aligned16(v)) || (lse && !aligned16(lse)))
+        return fail(CSA_ERR_ALIGNMENT, "attention pointer not 16-byte aligned");
+    return CSA_OK;
+}
+
+template <typename TIO>
+static csa_status_t run_attn(int mode, int B, int n_q, int64_t q_pos0, int m, long long window, long long N_kv, int H,
+                             int d, int k, float scale, const void* q, const void* kp, const void* vp, const int32_t* topk,
+                             void* out, float* lse, int splits, void* ws, cudaStream_t s)
+{
+    AttnArgsT<TIO> a{};
+    a.q = reinterpret_cast<const TIO*>(q);
+    a.k_ptr = reinterpret_cast<const TIO*>(kp);
+    a.v_ptr = reinterpret_cast<const TIO*>(vp);
+    a.out = reinterpret_cast<TIO*>(out);
+    a.lse = lse;
+    a.topk = topk;
+    a.q_pos0 = q_pos0;
+    a.window = window;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.mode = mode;
+    a.B = B;
+    a.n_q = n_q;
+    a.N_kv = (int)N_kv;
+    a.k = k;
+    a.m = m;
+    a.n_splits = splits;
+    if (splits > 1) {
+        a.part_o = reinterpret_cast<float*>(ws);
+        a.part_ml = a.part_o + (size_t)splits * B * n_q * H * d;
+    }
+    return cuda_status(launch_attn_simt<TIO>(a, H, d, s), "attention launch");
+}
+
+static size_t sparse_ws(int B, int n_q, int H, int d, int k)
+{
+    const int sp = attn_splits(n_q, k);
+    if (sp <= 1) return 0;
+    return (size_t)sp * B * n_q * H * (d + 2) * sizeof(float);
+}
+
+static csa_status_t check_index_args(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
+                                     const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
+                                     csa_dtype_t k_dtype, const void* k_scale)
+{
+    if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || H_I < 1 || d_I < 1 || q_pos0 < 0)
+        return fail(CSA_ERR_INVALID_ARG, "bad sizes");
+    csa_status_t st = check_index_dtypes(q_dtype, k_dtype, H_I, d_I);
+    if (st != CSA_OK) return st;
+    if ((long long)B * n_q * N_c == 0) return CSA_OK;
+    if (!q_idx || !k_idx) return fail(CSA_ERR_INVALID_ARG, "NULL q or k");
+    if (!aligned16(q_idx) || !aligned16(k_idx) || (q_scale && !aligned16(q_scale)) || (k_scale && !aligned16(k_scale)))
+        return fail(CSA_ERR_ALIGNMENT, "indexer pointer not 16-byte aligned");
+    if (q_dtype == CSA_E4M3 && !q_scale) return fail(CSA_ERR_INVALID_ARG, "E4M3 queries need q_scale");
+    if ((k_dtype == CSA_E4M3 || k_dtype == CSA_E2M1) && !k_scale)
+        return fail(CSA_ERR_INVALID_ARG, "quantised keys need k_scale");
+    if (k_dtype == CSA_E2M1 && d_I % 32) return fail(CSA_ERR_INVALID_ARG, "E2M1 keys need d_I % 32 == 0");
+    return CSA_OK;
+}
+
+static csa_status_t check_topk(int N_c, int k)
+{
+    if (k < 1 || k > 4096) return fail(CSA_ERR_UNSUPPORTED, "k=%d outside [1, 4096]", k);
+    TopkPlan p = topk_plan(N_c, k);
+    if (p.n_chunks > 1 && (long long)p.n_chunks * k > TOPK_MAX_MERGE)
+        return fail(CSA_ERR_UNSUPPORTED, "N_c=%d with k=%d exceeds the selection capacity", N_c, k);
+    return CSA_OK;
+}
+
+extern "C" {
+
+const char* csa_last_error(void) { return g_msg; }
+
+csa_status_t csa_device_status(csa_stream_t stream)
+{
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e, "cudaStreamSynchronize");
+    unsigned v = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&v, csa::g_status, sizeof(v));
+    if (e != cudaSuccess) return cuda_status(e, "read status word");
+    if (v) {
+        e = cudaMemcpyToSymbol(csa::g_status, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_status(e, "clear status word");
+    }
+    if (v & STATUS_TIMEOUT) return fail(CSA_ERR_TIMEOUT, "a device wait exceeded its time limit");
+    if (v & STATUS_BOUNDS) return fail(CSA_ERR_DEVICE, "a device-side bounds check failed");
+    return CSA_OK;
+}
+
+csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_streams, const void* const* x,
+                          const csa_dtype_t* x_dtype, const int* dim, void* const* out, const csa_dtype_t* out_dtype,
+                          void* const* out_scale, csa_stream_t stream)
+{
+    if (B < 0 || n < 0 || m < 1) return fail(CSA_ERR_INVALID_ARG, "bad sizes B=%d n=%d m=%d", B, n, m);
+    if (n_streams < 1 || n_streams > 4 || !x || !x_dtype || !dim || !out || !out_dtype)
+        return fail(CSA_ERR_INVALID_ARG, "bad stream arrays (n_streams=%d)", n_streams);
+    const int Nc = n / m;
+    if ((long long)B * Nc == 0) return CSA_OK;
+    if (!logits) return fail(CSA_ERR_INVALID_ARG, "logits is NULL");
+    if (!aligned16(logits)) return fail(CSA_ERR_ALIGNMENT, "logits not 16-byte aligned");
+    for (int s = 0; s < n_streams; ++s) {
+        const int d = dim[s];
+        const bool pow2 = d >= 8 && d <= 256 && (d & (d - 1)) == 0;
+        if (!pow2) return fail(CSA_ERR_UNSUPPORTED, "stream %d: dim %d not a power of two in [8, 256]", s, d);
+        if (x_dtype[s] != CSA_F32 && x_dtype[s] != CSA_BF16)
+            return fail(CSA_ERR_INVALID_ARG, "stream %d: input dtype must be F32 or BF16", s);
+        if (!x[s] || !out[s]) return fail(CSA_ERR_INVALID_ARG, "stream %d: NULL pointer", s);
+        if (!aligned16(x[s]) || !aligned16(out[s])) return fail(CSA_ERR_ALIGNMENT, "stream %d: pointer not 16-byte aligned", s);
+        const csa_dtype_t od = out_dtype[s];
+        if (od == CSA_E4M3 || od == CSA_E2M1) {
+            if (!out_scale || !out_scale[s]) return fail(CSA_ERR_INVALID_ARG, "stream %d: quantised output needs out_scale", s);
+            if (od == CSA_E4M3 && !aligned16(out_scale[s])) return fail(CSA_ERR_ALIGNMENT, "stream %d: scale not aligned", s);
+            if (od == CSA_E2M1 && d < 32) return fail(CSA_ERR_UNSUPPORTED, "stream %d: E2M1 needs dim >= 32", s);
+        } else if (od != CSA_F32 && od != CSA_BF16) {
+            return fail(CSA_ERR_INVALID_ARG, "stream %d: bad output dtype", s);
+        }
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    for (int s = 0; s < n_streams; ++s) {
+        const int kind = out_dtype[s] == CSA_F32 ? 0 : out_dtype[s] == CSA_BF16 ? 1 : out_dtype[s] == CSA_E4M3 ? 2 : 3;
+        cudaError_t e = launch_compress(B, n, m, dim[s], logits, x[s], x_dtype[s] == CSA_BF16, out[s], kind,
+                                        out_scale ? out_scale[s] : nullptr, st);
+        if (e != cudaSuccess) return cuda_status(e, "compress launch");
+    }
+    return CSA_OK;
+}
+
+size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dtype)
+{
+    if (B < 0 || N_c < 0 || d_I < 0) return 0;
+    return scores_ws_bytes(B, N_c, d_I, k_dtype);
+}
+
+
+csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, const void* q_idx,
+                              csa_dtype_t q_dtype, const float* q_scale, const void* k_idx, csa_dtype_t k_dtype,
+                              const void* k_scale, float* scores, void* workspace, size_t workspace_bytes,
+                              csa_stream_t stream)
+{
+    csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale);
+    if (st != CSA_OK) return st;
+    if ((long long)B * n_q * N_c == 0) return CSA_OK;
+    if (!scores || !aligned16(scores)) return fail(CSA_ERR_ALIGNMENT, "scores NULL or not aligned");
+    const size_t need = scores_ws_bytes(B, N_c, d_I, k_dtype);
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+    return run_scores(B, n_q, 0, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+                      scores, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k)
+{
+    if (B < 0 || n_q < 0 || N_c < 0 || k < 1) return 0;
+    return topk_workspace_bytes(B * n_q, N_c, k);
+}
+
+
+csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int k, const float* scores,
+                             int32_t* topk, void* workspace, size_t workspace_bytes, csa_stream_t stream)
+{
+    if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes");
+    csa_status_t st = check_topk(N_c, k);
+    if (st != CSA_OK) return st;
+    if ((long long)B * n_q == 0) return CSA_OK;
+    if (!topk || !aligned16(topk) || (N_c > 0 && (!scores || !aligned16(scores))))
+        return fail(CSA_ERR_ALIGNMENT, "scores/topk NULL or not aligned");
+    const size_t need = topk_workspace_bytes(B * n_q, N_c, k);
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+    return cuda_status(launch_topk(scores, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, workspace,
+                                   reinterpret_cast<cudaStream_t>(stream)),
+                       "topk launch");
+}
+
+size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, int k, csa_dtype_t k_dtype)
+{
+    if (B < 0 || n_q < 0 || N_c < 0 || k < 1) return 0;
+    const int rows = index_chunk_rows(B, n_q, N_c);
+    return align_up((size_t)B * rows * N_c * 4, 256) + scores_ws_bytes(B, N_c, d_I, k_dtype) +
+           topk_workspace_bytes(B * rows, N_c, k);
+}
+
+csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
+                            const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
+                            csa_dtype_t k_dtype, const void* k_scale, int32_t* topk, void* workspace,
+                            size_t workspace_bytes, csa_stream_t stream)
+{
+    csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale);
+    if (st != CSA_OK) return st;
+    st = check_topk(N_c, k);
+    if (st != CSA_OK) return st;
+    if ((long long)B * n_q == 0) return CSA_OK;
+    if (!topk || !aligned16(topk)) return fail(CSA_ERR_ALIGNMENT, "topk NULL or not aligned");
+    const size_t need = csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace))
+        return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int rows = index_chunk_rows(B, n_q, N_c);
+    uint8_t* w = reinterpret_cast<uint8_t*>(workspace);
+    float* scores = reinterpret_cast<float*>(w);
+    uint8_t* w_scores_ws = w + align_up((size_t)B * rows * N_c * 4, 256);
+    uint8_t* w_topk = w_scores_ws + scores_ws_bytes(B, N_c, d_I, k_dtype);
+    for (int i0 = 0; i0 < n_q; i0 += rows) {
+        const int nr = std::min(rows, n_q - i0);
+        if (N_c > 0) {
+            st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+                            scores, w_scores_ws, s);
+            if (st != CSA_OK) return st;
+        }
+        st = cuda_status(launch_topk(scores, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk, s),
+                         "topk launch");
+        if (st != CSA_OK) return st;
+    }
+    return CSA_OK;
+}
+
+size_t csa_sparse_attn_workspace_size(int B, int n_q, int H, int d, int k)
+{
+    if (B < 0 || n_q < 0 || H < 1 || d < 1 || k < 1) return 0;
+    return sparse_ws(B, n_q, H, d, k);
+}
+
+csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float scale, const void* q, const void* k_c,
+                             const void* v_c, csa_dtype_t dtype, const int32_t* topk, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, csa_stream_t stream)
+{
+    csa_status_t st = check_attn(B, n_q, H, d, N_c, q, k_c, v_c, dtype, out, lse);
+    if (st != CSA_OK) return st;
+    if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
+    if ((long long)B * n_q == 0) return CSA_OK;
+    if (!topk || !aligned16(topk)) return fail(CSA_ERR_ALIGNMENT, "topk NULL or not aligned");
+    const int splits = attn_splits(n_q, k);
+    const size_t need = sparse_ws(B, n_q, H, d, k);
+    if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == CSA_BF16)
+        return run_attn<__nv_bfloat16>(0, B, n_q, 0, 1, 0, N_c, H, d, k, scale, q, k_c, v_c, topk, out, lse, splits, workspace, s);
+    return run_attn<float>(0, B, n_q, 0, 1, 0, N_c, H, d, k, scale, q, k_c, v_c, topk, out, lse, splits, workspace, s);
+}
+
+csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int d, float scale, const void* q,
+                      const void* k_c, const void* v_c, csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream)
+{
+    if (m < 1 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad m / q_pos0");
+    csa_status_t st = check_attn(B, n_q, H, d, N_c, q, k_c, v_c, dtype, out, lse);
+    if (st != CSA_OK) return st;
+    if ((long long)B * n_q == 0) return CSA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == CSA_BF16)
+        return run_attn<__nv_bfloat16>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, 1, nullptr, s);
+    return run_attn<float>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, 1, nullptr, s);
+}
+
+csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int H, int d, float scale, const void* q,
+                      const void* k, const void* v, csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream)
+{
+    if (window < 1 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad window / q_pos0");
+    csa_status_t st = check_attn(B, n_q, H, d, n_kv, q, k, v, dtype, out, lse);
+    if (st != CSA_OK) return st;
+    if ((long long)B * n_q == 0) return CSA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == CSA_BF16)
+        return run_attn<__nv_bfloat16>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, 1, nullptr, s);
+    return run_attn<float>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, 1, nullptr, s);
+}
+
+}  // extern "C"

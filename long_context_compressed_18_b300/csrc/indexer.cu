@@ -1,0 +1,370 @@
+// Lightning Indexer scores ("DeepSeek V4 技术解读" §2.1: indexer queries of 64
+// heads x 128 dims are scored against the compressed entries; §五: the QK path
+// runs in FP8/FP4).
+//
+//     s(t, j) = sk(j) * sum_h sq(t, h) * <q(t, h), k(j)>      for j < nv(t)
+//
+// tcgen05 kernel (BF16 x BF16 via kind::f16, E4M3 x E4M3 via kind::f8f6f4,
+// fp32 accumulation in tensor memory).  The contraction is laid out with the
+// keys on the MMA's M side and (token, head) pairs on its N side:
+//     D[128 keys, T*64] = K_tile[128 x 128] * Q_group[T*64 x 128]^T
+// so that each TMEM lane holds one key and the head sum of the epilogue is a
+// per-thread reduction over 64 columns (no cross-lane traffic).  T = 4 tokens
+// (N = 256) for prefill, T = 1 (N = 64) for decode.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads (the query group once,
+// then a ring of key tiles); warp 1 owns the TMEM allocation and issues the
+// MMAs from one thread; warps 2-5 drain TMEM (tcgen05.ld), apply the scales,
+// sum over heads and store fp32 scores.  Accumulators are multi-buffered in
+// TMEM so the MMA of tile i+1 overlaps the epilogue of tile i.  Every mbarrier
+// wait is bounded; on a timeout the CTA drains its copies and MMAs, frees
+// TMEM and exits with the device status word set.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+
+namespace idx {
+constexpr int THREADS = 192;
+constexpr int BLOCK_KEYS = 128;   // MMA M
+constexpr int HEADS = 64;         // indexer heads
+constexpr int DIM = 128;          // indexer head dim
+constexpr int ATOM_BYTES_ROW = 128;
+
+template <bool FP8, int T> struct Cfg {
+    static constexpr int N = HEADS * T;
+    static constexpr int ELEM = FP8 ? 1 : 2;
+    static constexpr int ATOMS = DIM * ELEM / ATOM_BYTES_ROW;  // 128-byte K-major column blocks
+    static constexpr int KSTEP_ELEMS = FP8 ? 32 : 16;          // K per MMA instruction
+    static constexpr int KSTEPS = DIM / KSTEP_ELEMS;
+    static constexpr int KSTEPS_PER_ATOM = KSTEPS / ATOMS;
+    static constexpr int Q_ATOM = N * ATOM_BYTES_ROW;
+    static constexpr int Q_BYTES = Q_ATOM * ATOMS;
+    static constexpr int K_ATOM = BLOCK_KEYS * ATOM_BYTES_ROW;
+    static constexpr int K_BYTES = K_ATOM * ATOMS;
+    static constexpr int STAGES = (T == 1) ? 6 : (FP8 ? 6 : 4);
+    static constexpr int ACC = (T == 1) ? 4 : 2;
+    static constexpr int TMEM_COLS = ACC * N;   // 256 or 512
+    static constexpr uint32_t IDESC = instr_desc(FP8 ? 0u : 1u, FP8 ? 0u : 1u, BLOCK_KEYS, N);
+    // barriers: full[STAGES], empty[STAGES], acc_full[ACC], acc_empty[ACC], q, mma_done
+    static constexpr int N_BARS = 2 * STAGES + 2 * ACC + 2;
+    static constexpr int SMEM = 1024 /*align slack*/ + Q_BYTES + STAGES * K_BYTES + N_BARS * 8 +
+                                T * HEADS * 4 + 64;
+};
+}  // namespace idx
+
+template <bool FP8, int T>
+__global__ void __launch_bounds__(idx::THREADS, 1) indexer_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    const float* __restrict__ q_scale, const float* __restrict__ k_scale, float* __restrict__ scores,
+    int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int n_splits,
+    int split_tiles)
+{
+    using C = idx::Cfg<FP8, T>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = base;
+    uint8_t* sK = sQ + C::Q_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sK + C::STAGES * C::K_BYTES);
+    uint64_t* bar_full = bars;
+    uint64_t* bar_empty = bars + C::STAGES;
+    uint64_t* bar_acc_full = bars + 2 * C::STAGES;
+    uint64_t* bar_acc_empty = bars + 2 * C::STAGES + C::ACC;
+    uint64_t* bar_q = bars + 2 * C::STAGES + 2 * C::ACC;
+    uint64_t* bar_mma_done = bar_q + 1;
+    float* sq_s = reinterpret_cast<float*>(bars + C::N_BARS);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sq_s + T * idx::HEADS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int g = blockIdx.x / n_splits, split = blockIdx.x % n_splits;
+    const int i0 = g * T;                                   // first token of the group (chunk-local)
+    const int i_last = min(i0 + T - 1, n_q_rows - 1);
+    long long nvl = (q_pos0 + i_start + i_last + 1) / m;
+    const int nv_last = (int)(nvl < Nc ? nvl : Nc);
+    const int total_tiles = (nv_last + idx::BLOCK_KEYS - 1) / idx::BLOCK_KEYS;
+    const int tile0 = split * split_tiles;
+    const int n_tiles = min(split_tiles, total_tiles - tile0);
+    if (n_tiles <= 0) return;  // uniform over the CTA
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
+        for (int a = 0; a < C::ACC; ++a) { mbar_init(&bar_acc_full[a], 1); mbar_init(&bar_acc_empty[a], 4); }
+        mbar_init(bar_q, 1);
+        mbar_init(bar_mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_q);
+            tma_prefetch_desc(&tmap_k);
+            const int qrow = (b * n_q_total + i_start + i0) * idx::HEADS;
+            mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
+            for (int a = 0; a < C::ATOMS; ++a)
+                tma_load_2d(sQ + a * C::Q_ATOM, &tmap_q, bar_q, a * (idx::ATOM_BYTES_ROW / C::ELEM), qrow);
+            int issued = 0;
+            for (int li = 0; li < n_tiles; ++li) {
+                const int st = li % C::STAGES;
+                const uint32_t ph = (li / C::STAGES) & 1;
+                if (!mbar_wait(&bar_empty[st], ph ^ 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&bar_full[st], C::K_BYTES);
+                const int krow = b * Nc + (tile0 + li) * idx::BLOCK_KEYS;
+                uint8_t* dst = sK + st * C::K_BYTES;
+                for (int a = 0; a < C::ATOMS; ++a)
+                    tma_load_2d(dst + a * C::K_ATOM, &tmap_k, &bar_full[st], a * (idx::ATOM_BYTES_ROW / C::ELEM), krow);
+                issued = li + 1;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA exits
+                mbar_wait(bar_q, 0);
+                for (int li = max(0, issued - C::STAGES); li < issued; ++li)
+                    mbar_wait(&bar_full[li % C::STAGES], (li / C::STAGES) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (one thread) ----------------
+        if (lane == 0) {
+            const uint32_t sQ_addr = smem_u32(sQ);
+            const uint32_t sK_addr = smem_u32(sK);
+            if (mbar_wait(bar_q, 0, abort_flag)) {
+                for (int li = 0; li < n_tiles; ++li) {
+                    const int st = li % C::STAGES;
+                    const int acc = li % C::ACC;
+                    if (!mbar_wait(&bar_full[st], (li / C::STAGES) & 1, abort_flag)) break;
+                    if (!mbar_wait(&bar_acc_empty[acc], ((li / C::ACC) & 1) ^ 1, abort_flag)) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * C::N;
+#pragma unroll
+                    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+                        const int atom = ks / C::KSTEPS_PER_ATOM;
+                        const uint32_t koff = (ks % C::KSTEPS_PER_ATOM) * 32;
+                        const uint64_t a_desc = smem_desc(sK_addr + st * C::K_BYTES + atom * C::K_ATOM + koff, 16, 1024, SWZ_128B);
+                        const uint64_t b_desc = smem_desc(sQ_addr + atom * C::Q_ATOM + koff, 16, 1024, SWZ_128B);
+                        if constexpr (FP8) umma_f8(d_tmem, a_desc, b_desc, C::IDESC, ks > 0);
+                        else umma_f16(d_tmem, a_desc, b_desc, C::IDESC, ks > 0);
+                    }
+                    umma_commit(&bar_empty[st]);
+                    umma_commit(&bar_acc_full[acc]);
+                }
+            }
+            umma_commit(bar_mma_done);       // all MMAs of this CTA retired
+            mbar_wait(bar_mma_done, 0);
+        }
+    } else {
+        // ---------------- epilogue: 4 warps, one TMEM lane (= key) per thread ----
+        const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+        const int row = quad * 32 + lane;
+        const int et = threadIdx.x - 64;           // 0..127
+        for (int x = et; x < T * idx::HEADS; x += 128) {
+            const int tt = x / idx::HEADS, h = x % idx::HEADS;
+            const int i = i0 + tt;
+            float v = 0.f;
+            if (i < n_q_rows) v = q_scale ? q_scale[((long long)b * n_q_total + i_start + i) * idx::HEADS + h] : 1.f;
+            sq_s[x] = v;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int li = 0; li < n_tiles; ++li) {
+            const int acc = li % C::ACC;
+            const int key = (tile0 + li) * idx::BLOCK_KEYS + row;
+            const float sk = (k_scale && key < Nc) ? __ldg(k_scale + (long long)b * Nc + key) : 1.f;
+            const bool ok = mbar_wait(&bar_acc_full[acc], (li / C::ACC) & 1, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;   // tcgen05.ld below is warp-collective
+            tc_fence_after();
+#pragma unroll 1
+            for (int tt = 0; tt < T; ++tt) {
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::N + tt * idx::HEADS;
+                tmem_ld32(taddr, v0);
+                tmem_ld32(taddr + 32, v1);
+                tmem_ld_wait();
+                const float* sq = sq_s + tt * idx::HEADS;
+                float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                    p0 = fmaf(sq[h], __uint_as_float(v0[h]), p0);
+                    p1 = fmaf(sq[h + 1], __uint_as_float(v0[h + 1]), p1);
+                    p2 = fmaf(sq[h + 2], __uint_as_float(v0[h + 2]), p2);
+                    p3 = fmaf(sq[h + 3], __uint_as_float(v0[h + 3]), p3);
+                }
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                    p0 = fmaf(sq[32 + h], __uint_as_float(v1[h]), p0);
+                    p1 = fmaf(sq[33 + h], __uint_as_float(v1[h + 1]), p1);
+                    p2 = fmaf(sq[34 + h], __uint_as_float(v1[h + 2]), p2);
+                    p3 = fmaf(sq[35 + h], __uint_as_float(v1[h + 3]), p3);
+                }
+                const float s = ((p0 + p1) + (p2 + p3)) * sk;
+                const int i = i0 + tt;
+                if (i < n_q_rows) {
+                    long long nvt = (q_pos0 + i_start + i + 1) / m;
+                    if (key < nvt && key < Nc)
+                        scores[((long long)b * n_q_rows + i) * Nc + key] = s;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_acc_empty[acc]);
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fp32 scores on CUDA cores (any H_I, d_I): one thread per (query, entry).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) indexer_f32_kernel(
+    const float* __restrict__ q, const float* __restrict__ q_scale, const float* __restrict__ k,
+    const float* __restrict__ k_scale, float* __restrict__ scores, int n_q_total, int i_start,
+    int n_q_rows, long long q_pos0, int m, int Nc, int HI, int dI)
+{
+    extern __shared__ float qs[];
+    const int r = blockIdx.y;          // chunk-local row = b * n_q_rows + i
+    const int b = r / n_q_rows, i = r % n_q_rows;
+    const long long qrow = (long long)b * n_q_total + i_start + i;
+    for (int x = threadIdx.x; x < HI * dI; x += blockDim.x) qs[x] = q[qrow * HI * dI + x];
+    if (q_scale)
+        for (int x = threadIdx.x; x < HI; x += blockDim.x) qs[HI * dI + x] = q_scale[qrow * HI + x];
+    __syncthreads();
+    long long nvl = (q_pos0 + i_start + i + 1) / m;
+    const int nv = (int)(nvl < Nc ? nvl : Nc);
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= nv) return;
+    const float* kr = k + ((long long)b * Nc + j) * dI;
+    const float sk = k_scale ? k_scale[(long long)b * Nc + j] : 1.f;
+    float s = 0.f;
+    for (int h = 0; h < HI; ++h) {
+        float dot = 0.f;
+        for (int c = 0; c < dI; ++c) dot = fmaf(qs[h * dI + c], __ldg(kr + c), dot);
+        const float sq = q_scale ? qs[HI * dI + h] : 1.f;
+        s = fmaf(sq * sk, dot, s);
+    }
+    scores[(long long)r * Nc + j] = s;
+}
+
+// ---------------------------------------------------------------------------
+// FP4 (E2M1) -> FP8 (E4M3) widening of indexer keys ("DeepSeek V4 技术解读"
+// §五): per row S = 2^(floor(log2 max_b sc_b) - 5); x8 = E4M3(e * sc_b / S).
+// e * sc_b is exact in fp32 and S is a power of two, so the E4M3 conversion
+// is the only rounding.  One thread per 32-element block.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) fp4_to_e4m3_kernel(const uint8_t* __restrict__ packed,
+                                                          const uint8_t* __restrict__ sc,
+                                                          uint8_t* __restrict__ x8, float* __restrict__ S,
+                                                          long long rows, int d)
+{
+    const int nb = d / 32;
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= rows * nb) return;
+    const long long r = t / nb;
+    const int blk = (int)(t % nb);
+    float mx = 0.f;
+    for (int q = 0; q < nb; ++q) mx = fmaxf(mx, e4m3x2_to_f32x2(sc[r * nb + q]).x);
+    const int ex = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127;   // floor(log2 mx), mx normal
+    const float inv_S = __uint_as_float((uint32_t)(127 - (ex - 5)) << 23);
+    const float scb = e4m3x2_to_f32x2(sc[r * nb + blk]).x;
+    const uint4 p = *reinterpret_cast<const uint4*>(packed + r * (d / 2) + blk * 16);
+    const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+    uint32_t outw[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float v[8];
+        e2m1x8_to_f32x8(w[q], v);
+#pragma unroll
+        for (int c = 0; c < 8; c += 4) {
+            const uint32_t lo = f32x2_to_e4m3x2(__fmul_rn(__fmul_rn(v[c], scb), inv_S),
+                                                __fmul_rn(__fmul_rn(v[c + 1], scb), inv_S));
+            const uint32_t hi = f32x2_to_e4m3x2(__fmul_rn(__fmul_rn(v[c + 2], scb), inv_S),
+                                                __fmul_rn(__fmul_rn(v[c + 3], scb), inv_S));
+            outw[2 * q + c / 4] = lo | (hi << 16);
+        }
+    }
+    uint4* o = reinterpret_cast<uint4*>(x8 + r * d + blk * 32);
+    o[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+    o[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+    if (blk == 0) S[r] = __uint_as_float((uint32_t)(127 + (ex - 5)) << 23);
+}
+
+cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t* x8, float* S,
+                               long long rows, int d, cudaStream_t s)
+{
+    const long long n = rows * (d / 32);
+    if (n == 0) return cudaSuccess;
+    fp4_to_e4m3_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(packed, sc, x8, S, rows, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
+                               float* scores, int B, int n_q_total, int i_start, int n_q_rows,
+                               long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s)
+{
+    if (B * n_q_rows == 0 || Nc == 0) return cudaSuccess;
+    dim3 grid((Nc + 255) / 256, B * n_q_rows);
+    size_t smem = (size_t)(HI * dI + HI) * sizeof(float);
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(indexer_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    indexer_f32_kernel<<<grid, 256, smem, s>>>(q, q_scale, k, k_scale, scores, n_q_total, i_start,
+                                               n_q_rows, q_pos0, m, Nc, HI, dI);
+    return cudaGetLastError();
+}
+
+template <bool FP8, int T>
+static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const float* q_scale,
+                             const float* k_scale, float* scores, int B, int n_q_total, int i_start,
+                             int n_q_rows, long long q_pos0, int m, int Nc, int num_sms, cudaStream_t s)
+{
+    using C = idx::Cfg<FP8, T>;
+    const int n_groups = (n_q_rows + T - 1) / T;
+    long long nv_max = (q_pos0 + i_start + n_q_rows) / m;
+    if (nv_max > Nc) nv_max = Nc;
+    const int tiles = (int)((nv_max + idx::BLOCK_KEYS - 1) / idx::BLOCK_KEYS);
+    if (tiles == 0 || n_groups == 0) return cudaSuccess;
+    // split the key range when there are too few query groups to fill the GPU
+    const int per_sm = (C::SMEM <= 113 * 1024) ? 2 : 1;
+    const long long target = (long long)num_sms * per_sm * 4;
+    int splits = (int)std::min<long long>(tiles, std::max<long long>(1, (target + (long long)B * n_groups - 1) / ((long long)B * n_groups)));
+    const int split_tiles = (tiles + splits - 1) / splits;
+    splits = (tiles + split_tiles - 1) / split_tiles;
+    auto kern = indexer_tc_kernel<FP8, T>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    dim3 grid(n_groups * splits, B);
+    kern<<<grid, idx::THREADS, C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, n_q_total, i_start, n_q_rows,
+                                             q_pos0, m, Nc, splits, split_tiles);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const float* q_scale, const float* k_scale, float* scores, int B,
+                              int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
+                              int num_sms, cudaStream_t s)
+{
+    if (fp8) {
+        if (T == 4) return launch_tc<true, 4>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, s);
+        return launch_tc<true, 1>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, s);
+    }
+    if (T == 4) return launch_tc<false, 4>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, s);
+    return launch_tc<false, 1>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, s);
+}
+
+int indexer_group_tokens(int n_q) { return n_q >= 4 ? 4 : 1; }
+int indexer_box_rows(int T) { return idx::HEADS * T; }
+
+}  // namespace csa

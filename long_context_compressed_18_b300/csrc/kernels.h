@@ -1,0 +1,62 @@
+// Launchers of the device kernels, called by the C-ABI layer (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <type_traits>
+
+namespace csa {
+
+// ---- compression ----
+// out_kind: 0 f32, 1 bf16, 2 e4m3 (+ fp32 row scale), 3 e2m1 (+ e4m3 block scales)
+cudaError_t launch_compress(int B, int n, int m, int d, const float* logits, const void* x, bool x_bf16,
+                            void* out, int out_kind, void* out_scale, cudaStream_t s);
+
+// ---- top-k ----
+constexpr int TOPK_MAX_SINGLE = 32768;   // entries one CTA selects from (keys in smem)
+constexpr int TOPK_MAX_MERGE = 16384;    // candidates one CTA merges (keys + indices in smem)
+struct TopkPlan { int chunk; int n_chunks; };
+TopkPlan topk_plan(int N_c, int k);
+size_t topk_workspace_bytes(int rows, int N_c, int k);
+cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
+                        int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
+                        cudaStream_t s);
+
+// ---- indexer ----
+int indexer_group_tokens(int n_q);
+int indexer_box_rows(int T);
+cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const float* q_scale, const float* k_scale, float* scores, int B,
+                              int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
+                              int num_sms, cudaStream_t s);
+cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
+                               float* scores, int B, int n_q_total, int i_start, int n_q_rows,
+                               long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s);
+cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t* x8, float* S,
+                               long long rows, int d, cudaStream_t s);
+
+// ---- attention ----
+template <typename TIO> struct AttnArgsT {
+    const TIO* q;        // [B, n_q, H, D]
+    const TIO* k_ptr;    // [B, N_kv, D]
+    const TIO* v_ptr;    // [B, N_kv, D]
+    TIO* out;            // [B, n_q, H, D]
+    float* lse;          // [B, n_q, H] or null
+    const int32_t* topk; // [B, n_q, k] (mode 0)
+    float* part_o;       // [n_splits, B*n_q, H, D] when n_splits > 1
+    float* part_ml;      // [n_splits, B*n_q, H, 2]
+    long long q_pos0, window;
+    float scale_log2;    // softmax scale * log2(e)
+    int mode;            // 0 sparse, 1 closed blocks, 2 window
+    int B, n_q, N_kv, k, m, n_splits;
+};
+bool attn_simt_supported(int H, int D);
+template <typename TIO>
+cudaError_t launch_attn_simt(const AttnArgsT<TIO>& a, int H, int D, cudaStream_t s);
+
+}  // namespace csa

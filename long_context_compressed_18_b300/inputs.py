@@ -134,3 +134,15 @@ def random_scores(rows: int, length: int, seed: int, tie_levels: int = 0) -> tor
         x[:, 1] = 0.0
         x[:, 3] = -0.0
     return x.contiguous()
+
+
+def random_e2m1_keys(B: int, N: int, d: int, seed: int):
+    """Packed E2M1 codes [B, N, d/2] (uniform random nibbles) and E4M3 block
+    scales [B, N, d/32] (torch's cast of |N(0,1)|/6 + 1/64, so every block has a
+    positive scale with varied mantissas and exponents)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    packed = torch.randint(0, 256, (B, N, d // 2), generator=g, dtype=torch.int64).to(torch.uint8)
+    s = torch.randn(B, N, d // 32, generator=g).abs() / 6.0 + 1.0 / 64
+    sc = s.to(torch.float8_e4m3fn).view(torch.uint8)
+    return packed.contiguous(), sc.contiguous()
