@@ -143,7 +143,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
-    const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
+    // phase A / single pass: one CTA per (row, chunk); phase B: one CTA per row
+    const int r = (MODE == 0) ? (int)(blockIdx.x / n_chunks) : (int)blockIdx.x;
+    const int c = (MODE == 0) ? (int)(blockIdx.x % n_chunks) : 0;
     const int i = r % n_q_rows;   // query index within the chunk of rows
     const long long out_row = (long long)(r / n_q_rows) * out_b_stride + i;
     long long nvl = (q_pos0 + i + 1) / m;
