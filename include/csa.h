@@ -129,6 +129,31 @@ csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int
                              void* workspace, size_t workspace_bytes, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * csa_topk_select_noalloc -- the same selection as csa_topk_select, for
+ * callers that cannot allocate device memory: a plugin inside another
+ * runtime that owns all of the device's memory and passes this library only
+ * its input and output buffers, or a latency-critical path where a
+ * cudaMalloc, which can synchronise the device, is not acceptable.  The
+ * method's description has no counterpart of this call; it is an addition of
+ * this library.
+ *   Arguments and results as in csa_topk_select, without the workspace.
+ *   Scratch: a fixed device array of CSA_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB)
+ *   inside the library, enough for B * n_q * ceil(N_c / chunk) * k * 8 bytes
+ *   of candidates (csa_topk_select_workspace_size reports the need) -- e.g.
+ *   32 queries over 262,144 entries with k = 1024.  Larger selections return
+ *   CSA_ERR_WORKSPACE and launch nothing.  Every GPU that loads the library
+ *   holds the array until the process exits.
+ *   The call allocates nothing.  Its first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress) with that device current;
+ *   make that first call before any stream capture.  All calls on a device
+ *   share the one array and it keeps the last call's contents, so calls that
+ *   overlap on the GPU (several streams or host threads) race: serialise them.
+ * ------------------------------------------------------------------------- */
+#define CSA_TOPK_NOALLOC_SCRATCH_BYTES (4u << 20)
+csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, int m, int N_c, int k,
+                                     const float* scores, int32_t* topk, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * csa_index_topk -- scores and selection in one call (csa_index_scores then
  * csa_topk_select), processing the queries in chunks so that the score
  * buffer stays within the workspace.  Arguments as above.

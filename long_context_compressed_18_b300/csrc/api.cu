@@ -168,6 +168,11 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos
 
 }  // namespace
 
+namespace csa {
+// Sets the thread's last-error message for entry points defined in other files.
+csa_status_t report(csa_status_t st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace csa
+
 // ---------------------------------------------------------------------------
 // attention
 // ---------------------------------------------------------------------------

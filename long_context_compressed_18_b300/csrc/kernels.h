@@ -10,7 +10,12 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "../../include/csa.h"
+
 namespace csa {
+
+// Records the thread's last-error message (api.cu) and returns st.
+csa_status_t report(csa_status_t st, const char* msg);
 
 // ---- compression ----
 // out_kind: 0 f32, 1 bf16, 2 e4m3 (+ fp32 row scale), 3 e2m1 (+ e4m3 block scales)

@@ -1,0 +1,77 @@
+// csa_topk_select_noalloc: the top-k selection of csa_topk_select for callers
+// that cannot allocate device memory -- for example a plugin running inside
+// another runtime that owns all of the device's memory and hands this library
+// only its input and output buffers, or a latency-critical path where a
+// cudaMalloc, which can synchronise the device, is not acceptable.
+//
+// Instead of a caller-provided workspace, the candidate buffer of the
+// two-phase selection lives in a fixed file-scope device array.  Every GPU
+// that loads this library holds that array until the process exits.
+#include <mutex>
+
+#include "../../include/csa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// Scratch shared by every call on a device.  Sized for the 1M-context decode
+// shape: 32 rows x 16 chunks x 1024 candidates x (4-byte key + 4-byte index).
+static __device__ __align__(256) uint8_t g_topk_scratch[CSA_TOPK_NOALLOC_SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[MAX_DEVICES] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the symbol g_topk_scratch is only a host-side stand-in, never a device
+// address, so it is looked up here once per device, with that device current.
+csa_status_t scratch_address(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return csa::report(CSA_ERR_CUDA, "cudaGetDevice failed");
+    if (dev < 0 || dev >= MAX_DEVICES) return csa::report(CSA_ERR_UNSUPPORTED, "device index out of range");
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_topk_scratch);
+        if (e != cudaSuccess || !p)
+            return csa::report(CSA_ERR_CUDA, "cudaGetSymbolAddress of the top-k scratch array failed");
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, int m, int N_c, int k,
+                                                const float* scores, int32_t* topk, csa_stream_t stream)
+{
+    if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || q_pos0 < 0) return csa::report(CSA_ERR_INVALID_ARG, "bad sizes");
+    if (k < 1 || k > 4096) return csa::report(CSA_ERR_UNSUPPORTED, "k outside [1, 4096]");
+    const csa::TopkPlan plan = csa::topk_plan(N_c, k);
+    if (plan.n_chunks > 1 && (long long)plan.n_chunks * k > csa::TOPK_MAX_MERGE)
+        return csa::report(CSA_ERR_UNSUPPORTED, "N_c with this k exceeds the selection capacity");
+    if ((long long)B * n_q == 0) return CSA_OK;
+    if (!topk || (reinterpret_cast<uintptr_t>(topk) & 15u) ||
+        (N_c > 0 && (!scores || (reinterpret_cast<uintptr_t>(scores) & 15u))))
+        return csa::report(CSA_ERR_ALIGNMENT, "scores/topk NULL or not 16-byte aligned");
+    const size_t need = csa::topk_workspace_bytes(B * n_q, N_c, k);
+    if (need > (size_t)CSA_TOPK_NOALLOC_SCRATCH_BYTES)
+        return csa::report(CSA_ERR_WORKSPACE,
+                           "selection needs more scratch than the built-in 4 MiB array "
+                           "(CSA_TOPK_NOALLOC_SCRATCH_BYTES); use csa_topk_select with a workspace");
+    void* scratch = nullptr;
+    if (need > 0) {
+        const csa_status_t st = scratch_address(&scratch);
+        if (st != CSA_OK) return st;
+    }
+    // Nothing in the scratch has to start at zero: within one call, phase A
+    // writes every candidate slot that phase B then reads.
+    const cudaError_t e = csa::launch_topk(scores, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, scratch,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return csa::report(CSA_ERR_CUDA, cudaGetErrorString(e));
+    return CSA_OK;
+}

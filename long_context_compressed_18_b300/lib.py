@@ -21,7 +21,8 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "WORKS
           5: "CUDA", 6: "TIMEOUT", 7: "DEVICE"}
 
 EXPORTS = ("csa_compress", "csa_index_scores_workspace_size", "csa_index_scores",
-           "csa_topk_select_workspace_size", "csa_topk_select", "csa_index_topk_workspace_size",
+           "csa_topk_select_workspace_size", "csa_topk_select", "csa_topk_select_noalloc",
+           "csa_index_topk_workspace_size",
            "csa_index_topk", "csa_sparse_attn_workspace_size", "csa_sparse_attn", "hca_attn",
            "swa_attn", "csa_device_status", "csa_last_error")
 
@@ -50,6 +51,7 @@ def load():
         "csa_index_scores": ([_I, _I, _L, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _S, _P], _I),
         "csa_topk_select_workspace_size": ([_I, _I, _I, _I], _S),
         "csa_topk_select": ([_I, _I, _L, _I, _I, _I, _P, _P, _P, _S, _P], _I),
+        "csa_topk_select_noalloc": ([_I, _I, _L, _I, _I, _I, _P, _P, _P], _I),
         "csa_index_topk_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
         "csa_index_topk": ([_I, _I, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _S, _P], _I),
         "csa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I], _S),
@@ -119,6 +121,15 @@ def csa_topk_select_workspace_size(B, n_q, N_c, k):
 def csa_topk_select(B, n_q, q_pos0, m, N_c, k, scores, topk, workspace=None, workspace_bytes=0, stream=None):
     _check(load().csa_topk_select(B, n_q, q_pos0, m, N_c, k, _ptr(scores), _ptr(topk), _ptr(workspace),
                                   workspace_bytes, _stream(stream)))
+
+
+def csa_topk_select_noalloc(B, n_q, q_pos0, m, N_c, k, scores, topk, stream=None):
+    """csa_topk_select without a workspace, for callers that cannot allocate
+    device memory; the library uses its fixed built-in scratch array instead."""
+    _check(load().csa_topk_select_noalloc(B, n_q, q_pos0, m, N_c, k, _ptr(scores), _ptr(topk), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 def csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype):
