@@ -3,6 +3,7 @@
 // caller's stream.  No device memory is allocated here.
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -115,15 +116,18 @@ int index_chunk_rows(int B, int n_q, int N_c)
 }
 
 // Split-KV plan of the attention kernels.  Decode-shaped calls (few queries
-// per sequence) split each query's key set into slices of 128 so that one step
-// fills the GPU.  The plan depends only on the per-sequence shape, never on
-// the batch size, so a sequence's result is bitwise the same at any batch
+// per sequence) split each query's key set into slices of at least 256 keys
+// (a multiple of the tensor-core kernel's 128-key tile) so that one step fills
+// the GPU.  The plan depends only on the per-sequence shape, never on the
+// batch size, so a sequence's result is bitwise the same at any batch
 // position.
-int attn_splits(int n_q, long long set_len)
+struct SplitPlan { int n; int len; };
+SplitPlan attn_split_plan(int n_q, long long set_len)
 {
-    if (n_q > 16 || set_len <= 128) return 1;
-    long long s = (set_len + 127) / 128;
-    return (int)(s > 64 ? 64 : s);
+    if (n_q > 16 || set_len <= 256) return {1, 1 << 30};
+    long long len = 256;
+    while ((set_len + len - 1) / len > 64) len += 128;
+    return {(int)((set_len + len - 1) / len), (int)len};
 }
 
 csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos0, int m, int N_c, int H_I,
@@ -189,11 +193,56 @@ static csa_status_t check_attn(int B, int n_q, int H, int d, long long N_kv, con
     return CSA_OK;
 }
 
+static csa_status_t run_attn_tc(int mode, int B, int n_q, int64_t q_pos0, int m, long long window, long long N_kv,
+                               int H, int d, int k, float scale, const void* q, const void* kp, const void* vp,
+                               const int32_t* topk, void* out, float* lse, SplitPlan sp, void* ws, cudaStream_t s)
+{
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    csa_status_t st = make_map(&tq, q, bf, (uint64_t)d, (uint64_t)B * n_q * H, (uint64_t)d * 2, 64, 128);
+    if (st != CSA_OK) return st;
+    const uint32_t box = (uint32_t)attn_tc_box_rows(mode);
+    st = make_map(&tk, kp, bf, (uint64_t)d, (uint64_t)B * N_kv, (uint64_t)d * 2, 64, box);
+    if (st != CSA_OK) return st;
+    st = make_map(&tv, vp, bf, (uint64_t)d, (uint64_t)B * N_kv, (uint64_t)d * 2, 64, box);
+    if (st != CSA_OK) return st;
+    AttnTcParams p{};
+    p.topk = topk;
+    p.out = reinterpret_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    p.q_pos0 = q_pos0;
+    p.window = window;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.B = B;
+    p.n_q = n_q;
+    p.N_kv = (int)N_kv;
+    p.k = k;
+    p.m = m;
+    p.H = H;
+    p.T = attn_tc_tokens_per_cta(mode, H);
+    p.n_splits = sp.n;
+    p.split_len = sp.len;
+    if (sp.n > 1) {
+        p.part_o = reinterpret_cast<float*>(ws);
+        p.part_ml = p.part_o + (size_t)sp.n * B * n_q * H * d;
+    }
+    return cuda_status(launch_attn_tc(mode, tq, tk, tv, p, s), "attention (tcgen05) launch");
+}
+
 template <typename TIO>
 static csa_status_t run_attn(int mode, int B, int n_q, int64_t q_pos0, int m, long long window, long long N_kv, int H,
                              int d, int k, float scale, const void* q, const void* kp, const void* vp, const int32_t* topk,
-                             void* out, float* lse, int splits, void* ws, cudaStream_t s)
+                             void* out, float* lse, SplitPlan sp, void* ws, cudaStream_t s)
 {
+    if constexpr (std::is_same<TIO, __nv_bfloat16>::value) {
+        if (attn_tc_supported(H, d) && N_kv > 0) {
+            // TMA row coordinates are 32-bit
+            if ((long long)B * n_q * H + 128 > INT32_MAX || (long long)B * N_kv + 128 > INT32_MAX)
+                return fail(CSA_ERR_UNSUPPORTED, "attention tensors exceed 2^31 rows");
+            return run_attn_tc(mode, B, n_q, q_pos0, m, window, N_kv, H, d, k, scale, q, kp, vp, topk, out, lse, sp,
+                               ws, s);
+        }
+    }
     AttnArgsT<TIO> a{};
     a.q = reinterpret_cast<const TIO*>(q);
     a.k_ptr = reinterpret_cast<const TIO*>(kp);
@@ -210,19 +259,19 @@ static csa_status_t run_attn(int mode, int B, int n_q, int64_t q_pos0, int m, lo
     a.N_kv = (int)N_kv;
     a.k = k;
     a.m = m;
-    a.n_splits = splits;
-    if (splits > 1) {
+    a.n_splits = sp.n;
+    if (sp.n > 1) {
         a.part_o = reinterpret_cast<float*>(ws);
-        a.part_ml = a.part_o + (size_t)splits * B * n_q * H * d;
+        a.part_ml = a.part_o + (size_t)sp.n * B * n_q * H * d;
     }
     return cuda_status(launch_attn_simt<TIO>(a, H, d, s), "attention launch");
 }
 
 static size_t sparse_ws(int B, int n_q, int H, int d, int k)
 {
-    const int sp = attn_splits(n_q, k);
-    if (sp <= 1) return 0;
-    return (size_t)sp * B * n_q * H * (d + 2) * sizeof(float);
+    const SplitPlan sp = attn_split_plan(n_q, k);
+    if (sp.n <= 1) return 0;
+    return (size_t)sp.n * B * n_q * H * (d + 2) * sizeof(float);
 }
 
 static csa_status_t check_index_args(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
@@ -415,7 +464,7 @@ csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float
     if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
     if ((long long)B * n_q == 0) return CSA_OK;
     if (!topk || !aligned16(topk)) return fail(CSA_ERR_ALIGNMENT, "topk NULL or not aligned");
-    const int splits = attn_splits(n_q, k);
+    const SplitPlan splits = attn_split_plan(n_q, k);
     const size_t need = sparse_ws(B, n_q, H, d, k);
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
@@ -434,8 +483,8 @@ csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int
     if ((long long)B * n_q == 0) return CSA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == CSA_BF16)
-        return run_attn<__nv_bfloat16>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, 1, nullptr, s);
-    return run_attn<float>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, 1, nullptr, s);
+        return run_attn<__nv_bfloat16>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
+    return run_attn<float>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
 }
 
 csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int H, int d, float scale, const void* q,
@@ -447,8 +496,8 @@ csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int 
     if ((long long)B * n_q == 0) return CSA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == CSA_BF16)
-        return run_attn<__nv_bfloat16>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, 1, nullptr, s);
-    return run_attn<float>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, 1, nullptr, s);
+        return run_attn<__nv_bfloat16>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
+    return run_attn<float>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
 }
 
 }  // extern "C"

@@ -238,6 +238,14 @@ static cudaError_t launch_h(const AttnArgsT<TIO>& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
+cudaError_t launch_attn_combine(const AttnArgsT<__nv_bfloat16>& a, int H, int D, cudaStream_t s)
+{
+    const long long n = (long long)a.B * a.n_q * H * (D / 8);
+    if (n == 0) return cudaSuccess;
+    attn_combine_kernel<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, H, D);
+    return cudaGetLastError();
+}
+
 template <typename TIO, int D>
 static cudaError_t launch_d(const AttnArgsT<TIO>& a, int H, cudaStream_t s)
 {

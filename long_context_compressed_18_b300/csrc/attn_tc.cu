@@ -1,0 +1,481 @@
+// Attention of H query heads over one shared KV head on the tcgen05 tensor
+// cores (BF16 in, fp32 accumulate), for the three key sets of the hybrid
+// stack ("DeepSeek V4 技术解读"):
+//   mode 0  CSA core attention over the top-k selected entries (§2.1 Core
+//           Attention), the entries fetched with TMA row gathers,
+//   mode 1  HCA dense attention over all closed compressed blocks (§2.2),
+//   mode 2  sliding-window attention over raw tokens (§2.3).
+//
+// One CTA owns 128 (token, head) rows -- the M side of both products -- and
+// walks its key set in tiles of 128 keys:
+//     S   = Q K^T   A = Q  [128 rows x 128 dims]  smem, K-major, 128B swizzle
+//                   B = K  [128 keys x 128 dims]  smem, K-major
+//                   D = S  [128 lanes x 128 cols] fp32 in tensor memory
+//     O  += P V     A = P  [128 rows x 128 keys]  bf16 in tensor memory, over S
+//                   B = V  [128 keys x 128 dims]  smem, read MN-major
+//                   D = O  [128 lanes x 128 cols] fp32 in tensor memory
+// With every head in the M dimension each TMEM lane is one (token, head) row,
+// so the softmax (max, exponentials, row sum) is a per-thread loop with no
+// cross-thread reduction.  Rows are 2 tokens x 64 heads (dense modes) or one
+// token x H heads (sparse mode: every token has its own key set; with H = 64
+// the upper 64 rows idle).
+//
+// Warp roles (192 threads):
+//   warp 0     producer: Q once, then K and V tiles into a ring of STAGES
+//              buffers -- tiled TMA for the dense modes, tile::gather4 row
+//              gathers (4 selected rows per instruction, 32 lanes issuing)
+//              for the sparse mode, which also records a validity mask;
+//   warp 1     TMEM owner and single-thread MMA issuer: S_j into one of two S
+//              buffers, then O += P_{j-1} V_{j-1}, so the QK^T of tile j
+//              overlaps the softmax of tile j-1;
+//   warps 2-5  softmax and epilogue, one row per thread: online softmax in
+//              the base-2 domain against a lazily moved reference maximum,
+//              P written back to TMEM as bf16; O and l are rescaled (in TMEM)
+//              only when a row's maximum grows by more than 2^8.
+// Every mbarrier wait is bounded; on a timeout the CTA drains its copies and
+// MMAs, frees TMEM and exits with the device status word set.
+//
+// Split key sets (decode-shaped calls) write unnormalised partials (o, m, l)
+// that attn_combine_kernel merges in split order, so results stay
+// deterministic and independent of the batch size.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace csa {
+
+namespace atc {
+constexpr int THREADS = 192;
+constexpr int ROWS = 128;                 // MMA M
+constexpr int KT = 128;                   // keys per tile
+constexpr int D = 128;                    // head dim
+constexpr int ATOM = 128 * 128;           // 128 rows x 128 bytes (64 bf16 columns)
+constexpr int Q_BYTES = 2 * ATOM;
+constexpr int K_BYTES = 2 * ATOM;
+constexpr int V_BYTES = 2 * ATOM;
+constexpr int TMEM_COLS = 512;
+constexpr int S_COL = 0;                  // S buffers at columns 0 and 128
+constexpr int O_COL = 256;                // O accumulator at columns 256..383
+constexpr uint32_t IDESC_S = instr_desc(1u, 1u, ROWS, KT);          // bf16, both K-major
+constexpr uint32_t IDESC_PV = instr_desc(1u, 1u, ROWS, D, 0u, 1u);  // B (= V) MN-major
+constexpr uint32_t FULL = 0xFFFFFFFFu;
+
+template <int STAGES> struct Smem {
+    // barriers: q, mma_done, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full
+    static constexpr int N_BARS = 2 + 3 * STAGES + 5;
+    static constexpr int BYTES = 1024 + Q_BYTES + STAGES * (K_BYTES + V_BYTES) + N_BARS * 8 + STAGES * 16 + 16;
+};
+}  // namespace atc
+
+template <int MODE, int STAGES>
+__global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    const __grid_constant__ CUtensorMap tmap_v, const AttnTcParams p)
+{
+    using namespace atc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = base;
+    uint8_t* sK = sQ + Q_BYTES;
+    uint8_t* sV = sK + STAGES * K_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * V_BYTES);
+    uint64_t* bar_q = bars;
+    uint64_t* bar_mma_done = bars + 1;
+    uint64_t* k_full = bars + 2;
+    uint64_t* v_full = k_full + STAGES;
+    uint64_t* kv_empty = v_full + STAGES;
+    uint64_t* s_full = kv_empty + STAGES;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* o_full = p_full + 2;        // one phase per completed P_j V_j
+    uint32_t* kmask = reinterpret_cast<uint32_t*>(bars + Smem<STAGES>::N_BARS);   // [STAGES][4]
+    uint32_t* tmem_holder = kmask + 4 * STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int g = blockIdx.x / p.n_splits, split = blockIdx.x % p.n_splits;
+    const int i0 = g * p.T;                                  // first query token of the CTA
+    const int i_last = min(i0 + p.T, p.n_q) - 1;
+
+    // Key range of this CTA, in list positions (mode 0) or key indices.
+    long long set_lo = 0, set_len;
+    if (MODE == 0) {
+        set_len = p.k;
+    } else if (MODE == 1) {
+        const long long nv = (p.q_pos0 + i_last + 1) / p.m;
+        set_len = nv < p.N_kv ? nv : p.N_kv;
+    } else {
+        long long lo = p.q_pos0 + i0 - p.window + 1;
+        if (lo < 0) lo = 0;
+        long long hi = p.q_pos0 + i_last;
+        if (hi > p.N_kv - 1) hi = p.N_kv - 1;
+        set_lo = lo;
+        set_len = hi >= lo ? hi - lo + 1 : 0;
+    }
+    const long long r_lo = set_lo + (long long)split * p.split_len;
+    long long r_hi = set_lo + (long long)(split + 1) * p.split_len;
+    if (r_hi > set_lo + set_len) r_hi = set_lo + set_len;
+    const int n_tiles = r_hi > r_lo ? (int)((r_hi - r_lo + KT - 1) / KT) : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        mbar_init(bar_mma_done, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 4);
+        }
+        mbar_init(o_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (n_tiles > 0) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tmap_q);
+                tma_prefetch_desc(&tmap_k);
+                tma_prefetch_desc(&tmap_v);
+                const int qrow = (b * p.n_q + i0) * p.H;
+                mbar_arrive_expect_tx(bar_q, Q_BYTES);
+                tma_load_2d(sQ, &tmap_q, bar_q, 0, qrow);
+                tma_load_2d(sQ + ATOM, &tmap_q, bar_q, 64, qrow);
+            }
+            int issued = 0;
+            const int32_t* sel = (MODE == 0) ? p.topk + ((long long)b * p.n_q + i0) * p.k : nullptr;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % STAGES;
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(&kv_empty[st], ((j / STAGES) & 1) ^ 1, abort_flag);
+                if (!__shfl_sync(FULL, ok, 0)) break;
+                const long long pos0 = r_lo + (long long)j * KT;
+                if constexpr (MODE == 0) {
+                    int rows[4];
+                    uint32_t bal[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const long long pos = pos0 + 4 * lane + u;
+                        int idx = -1;
+                        if (pos < r_hi) idx = __ldg(sel + pos);
+                        if (idx >= p.N_kv || idx < -1) {
+                            flag_status(STATUS_BOUNDS);
+                            idx = -1;
+                        }
+                        const bool valid = idx >= 0;
+                        rows[u] = b * p.N_kv + (valid ? idx : 0);
+                        bal[u] = __ballot_sync(FULL, valid);
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) kmask[st * 4 + u] = bal[u];
+                        mbar_arrive_expect_tx(&k_full[st], K_BYTES);
+                        mbar_arrive_expect_tx(&v_full[st], V_BYTES);
+                    }
+                    __syncwarp();
+                    uint8_t* dk = sK + st * K_BYTES + lane * 512;
+                    uint8_t* dv = sV + st * V_BYTES + lane * 512;
+                    tma_gather4(dk, &tmap_k, &k_full[st], 0, rows[0], rows[1], rows[2], rows[3]);
+                    tma_gather4(dk + ATOM, &tmap_k, &k_full[st], 64, rows[0], rows[1], rows[2], rows[3]);
+                    tma_gather4(dv, &tmap_v, &v_full[st], 0, rows[0], rows[1], rows[2], rows[3]);
+                    tma_gather4(dv + ATOM, &tmap_v, &v_full[st], 64, rows[0], rows[1], rows[2], rows[3]);
+                } else {
+                    if (lane == 0) {
+                        const int krow = (int)((long long)b * p.N_kv + pos0);
+                        mbar_arrive_expect_tx(&k_full[st], K_BYTES);
+                        tma_load_2d(sK + st * K_BYTES, &tmap_k, &k_full[st], 0, krow);
+                        tma_load_2d(sK + st * K_BYTES + ATOM, &tmap_k, &k_full[st], 64, krow);
+                        mbar_arrive_expect_tx(&v_full[st], V_BYTES);
+                        tma_load_2d(sV + st * V_BYTES, &tmap_v, &v_full[st], 0, krow);
+                        tma_load_2d(sV + st * V_BYTES + ATOM, &tmap_v, &v_full[st], 64, krow);
+                    }
+                }
+                issued = j + 1;
+            }
+            if (lane == 0 && *abort_flag) {
+                // let the copies already in flight land before the CTA exits
+                mbar_wait(bar_q, 0);
+                for (int j = max(0, issued - STAGES); j < issued; ++j) {
+                    mbar_wait(&k_full[j % STAGES], (j / STAGES) & 1);
+                    mbar_wait(&v_full[j % STAGES], (j / STAGES) & 1);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------- MMA issuer ---------------------------
+        if (lane == 0 && n_tiles > 0) {
+            const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+            auto issue_pv = [&](int i) -> bool {
+                const int st = i % STAGES, sb = i & 1;
+                if (!mbar_wait(&v_full[st], (i / STAGES) & 1, abort_flag)) return false;
+                if (!mbar_wait(&p_full[sb], (i >> 1) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t a = tmem + S_COL + sb * KT;
+#pragma unroll
+                for (int ks = 0; ks < KT / 16; ++ks) {
+                    // 16 keys per step: 2 groups of 8 key rows (SBO = 1024 B);
+                    // the two 64-dim column blocks are one ATOM apart (LBO).
+                    const uint64_t b_desc = smem_desc(sVa + st * V_BYTES + ks * 2048, ATOM, 1024, SWZ_128B);
+                    umma_f16_tmem_a(tmem + O_COL, a + ks * 8, b_desc, IDESC_PV, (i > 0 || ks > 0) ? 1u : 0u);
+                }
+                umma_commit(&kv_empty[st]);
+                umma_commit(o_full);
+                return true;
+            };
+            bool ok = mbar_wait(bar_q, 0, abort_flag);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int st = j % STAGES, sb = j & 1;
+                if (!mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag)) { ok = false; break; }
+                // S buffer sb still holds P_{j-2} until P_{j-2} V_{j-2} has completed
+                if (j >= 2 && !mbar_wait(o_full, (j - 2) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + S_COL + sb * KT;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const int atom = ks / 4;
+                    const uint32_t koff = (ks % 4) * 32;
+                    const uint64_t a_desc = smem_desc(sQa + atom * ATOM + koff, 16, 1024, SWZ_128B);
+                    const uint64_t b_desc = smem_desc(sKa + st * K_BYTES + atom * ATOM + koff, 16, 1024, SWZ_128B);
+                    umma_f16(d, a_desc, b_desc, IDESC_S, ks > 0);
+                }
+                umma_commit(&s_full[sb]);
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok) issue_pv(n_tiles - 1);
+            umma_commit(bar_mma_done);      // all MMAs of this CTA retired
+            mbar_wait(bar_mma_done, 0);
+        }
+    } else {
+        // ----------------------- softmax + epilogue -----------------------
+        // Online softmax in the base-2 domain with a lazily moved reference
+        // maximum m_ref: P_j = 2^(s * scale * log2 e - m_ref) is accumulated
+        // by the tensor cores into O in TMEM; only when a row's tile maximum
+        // exceeds m_ref by more than 2^8 are O and l rescaled to the new
+        // maximum (so every P stays <= 256, exact enough in bf16).  The final
+        // o = O / l is the same for any choice of reference.
+        constexpr float RESCALE_LOG2 = 8.f;
+        const int quad = warp & 3;                       // TMEM lanes this warp may access
+        const int r = quad * 32 + lane;                  // row = TMEM lane
+        const int tt = r / p.H, h = r % p.H;
+        const int i = i0 + tt;
+        const bool row_ok = tt < p.T && i < p.n_q;
+        const bool warp_idle = __all_sync(FULL, !row_ok);
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float sl2 = p.scale_log2;
+
+        // Dense modes: the keys this row sees, as an absolute interval [ka, kb).
+        long long ka = 0, kb = 0;
+        if (MODE != 0 && row_ok) {
+            const long long t = p.q_pos0 + i;
+            if (MODE == 1) {
+                const long long nv = (t + 1) / p.m;
+                ka = r_lo;
+                kb = nv < r_hi ? nv : r_hi;
+            } else {
+                const long long lo = t - p.window + 1;
+                ka = lo > r_lo ? lo : r_lo;
+                kb = (t + 1) < r_hi ? (t + 1) : r_hi;
+            }
+        }
+
+        float m_ref = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j % STAGES, sb = j & 1;
+            bool w = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag);
+            if (MODE == 0 && w) w = mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag);  // orders the mask
+            if (!__all_sync(FULL, w)) { ok = false; break; }
+            tc_fence_after();
+            if (!warp_idle) {
+                // validity of column c: mode 0 bit (c / 4) of mask word (c % 4);
+                // dense modes c in [lo_c, hi_c)
+                uint32_t mk[4] = {0u, 0u, 0u, 0u};
+                int lo_c = 0, hi_c = 0;
+                if (MODE == 0) {
+                    if (row_ok) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) mk[u] = kmask[st * 4 + u];
+                    }
+                } else {
+                    const long long kbase = r_lo + (long long)j * KT;
+                    const long long a = ka - kbase, e = kb - kbase;
+                    lo_c = (int)(a < 0 ? 0 : (a > KT ? KT : a));
+                    hi_c = (int)(e < 0 ? 0 : (e > KT ? KT : e));
+                }
+                const uint32_t s_addr = tmem + lane_base + S_COL + sb * KT;
+                float sv[KT];
+#pragma unroll
+                for (int q = 0; q < KT / 32; ++q) tmem_ld32(s_addr + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
+                tmem_ld_wait();
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < KT; ++c) {
+                    const bool v = (MODE == 0) ? ((mk[c & 3] >> (c >> 2)) & 1u) : (c >= lo_c && c < hi_c);
+                    sv[c] = v ? sv[c] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, sv[c]);
+                }
+                // move the reference maximum if this tile exceeds it by > 2^8
+                const bool move = mx > m_ref + RESCALE_LOG2;
+                const float m_new = move ? mx : m_ref;
+                if (__any_sync(FULL, move && m_ref != -INFINITY)) {
+                    // O holds P_0..P_{j-1} V against the old reference: wait
+                    // for P_{j-1} V_{j-1}, then rescale the rows that moved
+                    const bool w2 = mbar_wait(o_full, (j - 1) & 1, abort_flag);
+                    if (!__all_sync(FULL, w2)) { ok = false; break; }
+                    tc_fence_after();
+                    const float f = (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
+                    const uint32_t o_addr = tmem + lane_base + O_COL;
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_addr + 32 * q, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
+                        tmem_st32(o_addr + 32 * q, ov);
+                    }
+                    l_run *= f;
+                }
+                m_ref = m_new;
+                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < KT / 32; ++q) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const float p0 = ex2_approx(sv[32 * q + 2 * u] + neg_m);
+                        const float p1 = ex2_approx(sv[32 * q + 2 * u + 1] + neg_m);
+                        sum += p0 + p1;
+                        pk[u] = pack_bf16x2(p0, p1);
+                    }
+                    // P columns 16q..16q+15 overwrite S columns already read
+                    tmem_st16(s_addr + 16 * q, pk);
+                }
+                tmem_st_wait();
+                l_run += sum;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[sb]);
+        }
+
+        if (ok && n_tiles > 0) {
+            // every MMA of the CTA has retired (a single-use barrier: the
+            // per-tile o_full phases cannot tell the last two tiles apart here)
+            const bool w = mbar_wait(bar_mma_done, 0, abort_flag);
+            ok = __all_sync(FULL, w);
+            if (ok) tc_fence_after();
+        }
+        if (ok && !warp_idle) {
+            const long long grow = ((long long)b * p.n_q + i) * p.H + h;   // (b, token, head)
+            const uint32_t o_addr = tmem + lane_base + O_COL;
+            const bool split_out = p.n_splits > 1;
+            const float inv = (!split_out && l_run > 0.f) ? 1.f / l_run : (split_out ? 1.f : 0.f);
+            const long long prow = (long long)split * p.B * p.n_q * p.H + grow;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t ov[32];
+                if (n_tiles > 0) {
+                    tmem_ld32(o_addr + 32 * q, ov);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) ov[u] = 0u;
+                }
+                if (!row_ok) continue;
+                if (!split_out) {
+                    uint4* op = reinterpret_cast<uint4*>(p.out + grow * D + 32 * q);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 w4;
+                        w4.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+                        w4.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+                        w4.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+                        w4.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+                        op[c / 8] = w4;
+                    }
+                } else {
+                    float4* po = reinterpret_cast<float4*>(p.part_o + prow * D + 32 * q);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        po[c / 4] = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
+                                                __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+                }
+            }
+            if (row_ok) {
+                if (!split_out) {
+                    if (p.lse) p.lse[grow] = l_run > 0.f ? (m_ref + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+                } else {
+                    p.part_ml[2 * prow] = l_run > 0.f ? m_ref : -INFINITY;
+                    p.part_ml[2 * prow + 1] = l_run;
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+constexpr int ATTN_TC_STAGES = 2;
+
+size_t attn_tc_smem_bytes() { return atc::Smem<ATTN_TC_STAGES>::BYTES; }
+
+bool attn_tc_supported(int H, int D) { return (H == 64 || H == 128) && D == atc::D; }
+
+int attn_tc_tokens_per_cta(int mode, int H) { return mode == 0 ? 1 : atc::ROWS / H; }
+
+int attn_tc_box_rows(int mode) { return mode == 0 ? 1 : atc::KT; }
+
+cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const AttnTcParams& p, cudaStream_t s)
+{
+    if ((long long)p.B * p.n_q == 0) return cudaSuccess;
+    const int n_groups = (p.n_q + p.T - 1) / p.T;
+    dim3 grid((unsigned)(n_groups * p.n_splits), (unsigned)p.B);
+    const int smem = (int)attn_tc_smem_bytes();
+    cudaError_t e;
+    if (mode == 0) {
+        auto kern = attn_tc_kernel<0, ATTN_TC_STAGES>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+    } else if (mode == 1) {
+        auto kern = attn_tc_kernel<1, ATTN_TC_STAGES>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+    } else {
+        auto kern = attn_tc_kernel<2, ATTN_TC_STAGES>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.n_splits == 1) return e;
+    AttnArgsT<__nv_bfloat16> a{};
+    a.out = p.out;
+    a.lse = p.lse;
+    a.part_o = p.part_o;
+    a.part_ml = p.part_ml;
+    a.B = p.B;
+    a.n_q = p.n_q;
+    a.n_splits = p.n_splits;
+    return launch_attn_combine(a, p.H, atc::D, s);
+}
+
+}  // namespace csa

@@ -63,5 +63,28 @@ template <typename TIO> struct AttnArgsT {
 bool attn_simt_supported(int H, int D);
 template <typename TIO>
 cudaError_t launch_attn_simt(const AttnArgsT<TIO>& a, int H, int D, cudaStream_t s);
+// merges split partials (a.part_o, a.part_ml) into a.out / a.lse
+cudaError_t launch_attn_combine(const AttnArgsT<__nv_bfloat16>& a, int H, int D, cudaStream_t s);
+
+// tcgen05 attention (BF16, D = 128, H in {64, 128}); tensor maps over
+// Q [B*n_q*H, 128], K / V [B*N_kv, 128], 64-column boxes with 128-byte swizzle
+// (Q box 128 rows; K / V box attn_tc_box_rows(mode) rows).
+struct AttnTcParams {
+    const int32_t* topk;   // [B, n_q, k] (mode 0)
+    __nv_bfloat16* out;    // [B, n_q, H, 128]
+    float* lse;            // [B, n_q, H] or null
+    float* part_o;         // [n_splits, B*n_q, H, 128] when n_splits > 1
+    float* part_ml;        // [n_splits, B*n_q, H, 2]
+    long long q_pos0, window;
+    float scale_log2;      // softmax scale * log2(e)
+    int B, n_q, N_kv, k, m, H;
+    int T;                 // query tokens per CTA
+    int n_splits, split_len;   // key-set slices of split_len (a multiple of 128)
+};
+bool attn_tc_supported(int H, int D);
+int attn_tc_tokens_per_cta(int mode, int H);
+int attn_tc_box_rows(int mode);
+cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const AttnTcParams& p, cudaStream_t s);
 
 }  // namespace csa
