@@ -326,32 +326,129 @@ def run_decode(args, torch, dist, rank, world):
 
 
 # ---------------------------------------------------------------------------
+def _pairs(s, window_or_k=None):
+    """Sum over the queries of the visible entries (or min(k, nv), or the window)."""
+    t = list(range(s.q_pos0, s.q_pos0 + s.n_q))
+    if s.kind == "swa":
+        return sum(min(s.window, tt + 1, s.n) for tt in t)
+    nv = [min((tt + 1) // s.m, s.N_c) for tt in t]
+    if window_or_k:
+        return sum(min(window_or_k, v) for v in nv)
+    return sum(nv)
+
+
 def run_config(args, torch, name):
-    """Per-call timing of another named workload (one rank)."""
-    from long_context_compressed_18_b300 import configs, inputs, pipeline
+    """Per-stage CUDA-event timing of a prefill workload (one rank): every
+    kernel of each layer is timed on its own, with its roofline fraction."""
+    import math as _m
+    from long_context_compressed_18_b300 import configs, inputs, lib, pipeline
     layers = configs.STACK_LAYERS if name == "stack" else (configs.NAMED[name],)
-    ws = pipeline.Workspace()
-    xs = [inputs.make_inputs(s, device="cuda") for s in layers]
+    peaks, peak_src = _peaks()
+    hbm = peaks["hbm_gbs"]
+    bf16_pf = peaks["bf16_tflops"]
     stream = torch.cuda.current_stream()
-    for _ in range(max(1, args.warmup)):
-        for s, x in zip(layers, xs):
-            pipeline.run_layer(x, s, ws)
-    torch.cuda.synchronize()
-    res = {}
+    code = {"f32": lib.F32, "bf16": lib.BF16, "e4m3": lib.E4M3, "e2m1": lib.E2M1}
+    stages_all = {}
     with ClockSampler(_gpu_id(torch, torch.cuda.current_device())) as clk:
-        for s, x in zip(layers, xs):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for _ in range(args.steps):
-                pipeline.run_layer(x, s, ws)
-            b.record(stream)
+        for s in layers:
+            x = inputs.make_inputs(s, device="cuda")
+            B, n, d, H = s.B, s.n, s.d, s.H
+            tau = 1.0 / _m.sqrt(d)
+            ebytes = 4 if s.dtype == "f32" else 2
+            st = {}
+            calls = []
+            if s.kind in ("csa", "hca"):
+                names = ["k", "v"] + (["idx_k"] if s.kind == "csa" else [])
+                kinds = [s.dtype, s.dtype] + ([s.idx_k_dtype] if s.kind == "csa" else [])
+                comp = {}
+
+                def do_compress(names=names, kinds=kinds, x=x, s=s, comp=comp):
+                    for nm, kd, (o, sc) in zip(names, kinds,
+                                               pipeline.compress(x["logits"], [x[nm] for nm in names], s.m, kinds)):
+                        comp[nm] = (o, sc)
+                Nc = s.N_c
+                cbytes = 0
+                for nm, kd in zip(names, kinds):
+                    dd = x[nm].shape[-1]
+                    ob = {"f32": 4, "bf16": 2, "e4m3": 1, "e2m1": 0.5}[kd] * dd + \
+                        {"f32": 0, "bf16": 0, "e4m3": 4, "e2m1": dd / 32}[kd]
+                    cbytes += B * (n * dd * x[nm].element_size() + n * 4 + Nc * ob)
+                calls.append(("compress", do_compress, cbytes, "GB/s", hbm))
+                do_compress()
+            if s.kind == "csa":
+                ik, iks = comp["idx_k"]
+                rows = s.n_q
+                scores = torch.empty(B, rows, s.N_c, dtype=torch.float32, device="cuda")
+                topk = torch.empty(B, rows, s.k, dtype=torch.int32, device="cuda")
+                wsb = lib.csa_index_scores_workspace_size(B, s.N_c, s.d_I, code[s.idx_k_dtype])
+                ws_i = lib.empty_workspace(wsb)
+                twsb = lib.csa_topk_select_workspace_size(B, rows, s.N_c, s.k)
+                ws_t = lib.empty_workspace(twsb)
+                pairs = B * _pairs(s)
+
+                def do_index(x=x, s=s, ik=ik, iks=iks, scores=scores, ws_i=ws_i, wsb=wsb, B=B, rows=rows):
+                    lib.csa_index_scores(B, rows, s.q_pos0, s.m, s.N_c, s.H_I, s.d_I, x["idx_q"],
+                                         code[s.idx_q_dtype], x["idx_q_scale"], ik, code[s.idx_k_dtype], iks,
+                                         scores, ws_i, wsb)
+
+                def do_topk(s=s, scores=scores, topk=topk, ws_t=ws_t, twsb=twsb, B=B, rows=rows):
+                    lib.csa_topk_select(B, rows, s.q_pos0, s.m, s.N_c, s.k, scores, topk, ws_t, twsb)
+                ipk = 2.0 if s.idx_q_dtype == "e4m3" else 1.0
+                calls.append(("indexer", do_index, 2.0 * s.H_I * s.d_I * pairs, "TFLOP/s", bf16_pf * ipk))
+                calls.append(("topk", do_topk, 4.0 * pairs, "GB/s", hbm))
+                kc, vc = comp["k"][0], comp["v"][0]
+                out = torch.empty_like(x["q"])
+                lse = torch.empty(B, s.n_q, H, dtype=torch.float32, device="cuda")
+                awsb = lib.csa_sparse_attn_workspace_size(B, s.n_q, H, d, s.k)
+                ws_a = lib.empty_workspace(awsb)
+
+                def do_attn(x=x, s=s, kc=kc, vc=vc, topk=topk, out=out, lse=lse, ws_a=ws_a, awsb=awsb):
+                    lib.csa_sparse_attn(B, s.n_q, H, d, s.N_c, s.k, tau, x["q"], kc, vc, code[s.dtype], topk, out,
+                                        lse, ws_a, awsb)
+                do_index(); do_topk()
+                calls.append(("sparse_attn", do_attn, 4.0 * H * d * B * _pairs(s, s.k), "TFLOP/s", bf16_pf))
+            elif s.kind == "hca":
+                kc, vc = comp["k"][0], comp["v"][0]
+                out = torch.empty_like(x["q"])
+                lse = torch.empty(B, s.n_q, H, dtype=torch.float32, device="cuda")
+
+                def do_hca(x=x, s=s, kc=kc, vc=vc, out=out, lse=lse):
+                    lib.hca_attn(B, s.n_q, s.q_pos0, s.m, s.N_c, H, d, tau, x["q"], kc, vc, code[s.dtype], out, lse)
+                calls.append(("hca_attn", do_hca, 4.0 * H * d * B * _pairs(s), "TFLOP/s", bf16_pf))
+            elif s.kind == "swa":
+                out = torch.empty_like(x["q"])
+                lse = torch.empty(B, s.n_q, H, dtype=torch.float32, device="cuda")
+
+                def do_swa(x=x, s=s, out=out, lse=lse):
+                    lib.swa_attn(B, s.n_q, s.q_pos0, s.n, s.window, H, d, tau, x["q"], x["k"], x["v"], code[s.dtype],
+                                 out, lse)
+                calls.append(("swa_attn", do_swa, 4.0 * H * d * B * _pairs(s), "TFLOP/s", bf16_pf))
+            for _ in range(max(1, args.warmup)):
+                for _, fn, _, _, _ in calls:
+                    fn()
             torch.cuda.synchronize()
-            res[s.name] = a.elapsed_time(b) / args.steps
-    tot = sum(res.values())
+            lib.csa_device_status()
+            for cname, fn, work, unit, peak in calls:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ms = a.elapsed_time(b) / args.steps
+                ach = work / (ms / 1e3) / (1e9 if unit == "GB/s" else 1e12)
+                st[cname] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": unit, "peak": peak,
+                             "frac": round(ach / peak, 4), "work_per_launch": work}
+            lib.csa_device_status()
+            stages_all[s.name] = st
+            del x, calls
+            torch.cuda.empty_cache()
+    tot = sum(v["ms"] for st in stages_all.values() for v in st.values())
     n_q = sum(s.B * s.n_q for s in layers)
-    return {"metric": "queries/s (prefill)", "value": n_q / (tot / 1e3), "unit": "queries/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot, "higher_is_better": True,
-            "config": {"workload": name}, "per_layer_ms": res, "clocks": clk.summary(), "data": "synthetic"}
+    return {"metric": "prefill queries/s (all stages of the workload)", "value": n_q / (tot / 1e3),
+            "unit": "queries/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot,
+            "higher_is_better": True, "config": {"workload": name}, "stages": stages_all,
+            "peak_source": peak_src, "clocks": clk.summary(), "data": "synthetic"}
 
 
 def run_reference(args, torch, rank, world):
