@@ -176,8 +176,12 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
  *          (CSA_F32 or CSA_BF16);  out  device [B, n_q, H, d] in dtype;
  *   topk   device int32 [B, n_q, k], entries in [0, N_c) or -1;
  *   lse    device fp32 [B, n_q, H] or NULL.
- * Requirements: d in {64, 128}, 1 <= H <= 128.  Indices outside [-1, N_c)
- * are skipped and flagged in the device status word.
+ * Requirements: d in {64, 128}, H in {8, 16, 32, 64, 128}, scale > 0 and
+ * finite (else CSA_ERR_INVALID_ARG).  Indices outside [-1, N_c) are skipped
+ * and flagged in the device status word.
+ * Precision: BF16 with d = 128 and H in {64, 128} runs on the tcgen05 tensor
+ * cores (the probabilities enter the P.V product rounded to bf16, fp32
+ * accumulation); other shapes and fp32 I/O run on CUDA cores in fp32.
  * ------------------------------------------------------------------------- */
 size_t csa_sparse_attn_workspace_size(int B, int n_q, int H, int d, int k);
 csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float scale,

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -180,10 +181,11 @@ csa_status_t report(csa_status_t st, const char* msg) { return fail(st, "%s", ms
 // ---------------------------------------------------------------------------
 // attention
 // ---------------------------------------------------------------------------
-static csa_status_t check_attn(int B, int n_q, int H, int d, long long N_kv, const void* q, const void* k,
+static csa_status_t check_attn(int B, int n_q, int H, int d, long long N_kv, float scale, const void* q, const void* k,
                                const void* v, csa_dtype_t dtype, const void* out, const float* lse)
 {
     if (B < 0 || n_q < 0 || N_kv < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes");
+    if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CSA_ERR_INVALID_ARG, "scale must be positive and finite");
     if (dtype != CSA_F32 && dtype != CSA_BF16) return fail(CSA_ERR_UNSUPPORTED, "attention dtype must be F32 or BF16");
     if (!attn_simt_supported(H, d)) return fail(CSA_ERR_UNSUPPORTED, "attention needs H in {8,16,32,64,128}, d in {64,128}");
     if ((long long)B * n_q == 0) return CSA_OK;
@@ -199,12 +201,13 @@ static csa_status_t run_attn_tc(int mode, int B, int n_q, int64_t q_pos0, int m,
 {
     CUtensorMap tq, tk, tv;
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    csa_status_t st = make_map(&tq, q, bf, (uint64_t)d, (uint64_t)B * n_q * H, (uint64_t)d * 2, 64, 128);
+    csa_status_t st = make_map(&tq, q, bf, (uint64_t)d, (uint64_t)B * n_q * H, (uint64_t)d * 2, 64,
+                               (uint32_t)attn_tc_q_box_rows(mode, H));
     if (st != CSA_OK) return st;
-    const uint32_t box = (uint32_t)attn_tc_box_rows(mode);
-    st = make_map(&tk, kp, bf, (uint64_t)d, (uint64_t)B * N_kv, (uint64_t)d * 2, 64, box);
+    const uint32_t kv_box = mode == 0 ? 1 : 128;     // row gathers vs 128-key tiles
+    st = make_map(&tk, kp, bf, (uint64_t)d, (uint64_t)B * N_kv, (uint64_t)d * 2, 64, kv_box);
     if (st != CSA_OK) return st;
-    st = make_map(&tv, vp, bf, (uint64_t)d, (uint64_t)B * N_kv, (uint64_t)d * 2, 64, box);
+    st = make_map(&tv, vp, bf, (uint64_t)d, (uint64_t)B * N_kv, (uint64_t)d * 2, 64, kv_box);
     if (st != CSA_OK) return st;
     AttnTcParams p{};
     p.topk = topk;
@@ -235,7 +238,8 @@ static csa_status_t run_attn(int mode, int B, int n_q, int64_t q_pos0, int m, lo
                              void* out, float* lse, SplitPlan sp, void* ws, cudaStream_t s)
 {
     if constexpr (std::is_same<TIO, __nv_bfloat16>::value) {
-        if (attn_tc_supported(H, d) && N_kv > 0) {
+        // the tensor-core kernel stages at most 4096 selected entries per CTA
+        if (attn_tc_supported(H, d) && N_kv > 0 && (mode != 0 || k <= 4096)) {
             // TMA row coordinates are 32-bit
             if ((long long)B * n_q * H + 128 > INT32_MAX || (long long)B * N_kv + 128 > INT32_MAX)
                 return fail(CSA_ERR_UNSUPPORTED, "attention tensors exceed 2^31 rows");
@@ -459,7 +463,7 @@ csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float
                              const void* v_c, csa_dtype_t dtype, const int32_t* topk, void* out, float* lse,
                              void* workspace, size_t workspace_bytes, csa_stream_t stream)
 {
-    csa_status_t st = check_attn(B, n_q, H, d, N_c, q, k_c, v_c, dtype, out, lse);
+    csa_status_t st = check_attn(B, n_q, H, d, N_c, scale, q, k_c, v_c, dtype, out, lse);
     if (st != CSA_OK) return st;
     if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
     if ((long long)B * n_q == 0) return CSA_OK;
@@ -478,7 +482,7 @@ csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int
                       const void* k_c, const void* v_c, csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream)
 {
     if (m < 1 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad m / q_pos0");
-    csa_status_t st = check_attn(B, n_q, H, d, N_c, q, k_c, v_c, dtype, out, lse);
+    csa_status_t st = check_attn(B, n_q, H, d, N_c, scale, q, k_c, v_c, dtype, out, lse);
     if (st != CSA_OK) return st;
     if ((long long)B * n_q == 0) return CSA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -491,7 +495,7 @@ csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int 
                       const void* k, const void* v, csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream)
 {
     if (window < 1 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad window / q_pos0");
-    csa_status_t st = check_attn(B, n_q, H, d, n_kv, q, k, v, dtype, out, lse);
+    csa_status_t st = check_attn(B, n_q, H, d, n_kv, scale, q, k, v, dtype, out, lse);
     if (st != CSA_OK) return st;
     if ((long long)B * n_q == 0) return CSA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -2,7 +2,7 @@
 // cores (BF16 in, fp32 accumulate), for the three key sets of the hybrid
 // stack ("DeepSeek V4 技术解读"):
 //   mode 0  CSA core attention over the top-k selected entries (§2.1 Core
-//           Attention), the entries fetched with TMA row gathers,
+//           Attention), the selected entries fetched with TMA row gathers,
 //   mode 1  HCA dense attention over all closed compressed blocks (§2.2),
 //   mode 2  sliding-window attention over raw tokens (§2.3).
 //
@@ -20,15 +20,18 @@
 // token x H heads (sparse mode: every token has its own key set; with H = 64
 // the upper 64 rows idle).
 //
-// Warp roles (192 threads):
-//   warp 0     producer: Q once, then K and V tiles into a ring of STAGES
-//              buffers -- tiled TMA for the dense modes, tile::gather4 row
-//              gathers (4 selected rows per instruction, 32 lanes issuing)
-//              for the sparse mode, which also records a validity mask;
-//   warp 1     TMEM owner and single-thread MMA issuer: S_j into one of two S
+// Warp roles (224 threads):
+//   warps 0-1  producers: Q once, then K and V tiles into rings of STAGES
+//              buffers (a K stage is released when S_j completes, a V stage
+//              when P_j V_j completes) -- tiled TMA for the dense modes; for
+//              the sparse mode TMA tile::gather4 row gathers (4 selected rows
+//              of 64 columns per instruction) issued by all 64 lanes of both
+//              warps: one warp's issue rate tops out near 7 bytes per cycle
+//              per SM, two reach the latency limit of the ring;
+//   warp 2     TMEM owner and single-thread MMA issuer: S_j into one of two S
 //              buffers, then O += P_{j-1} V_{j-1}, so the QK^T of tile j
 //              overlaps the softmax of tile j-1;
-//   warps 2-5  softmax and epilogue, one row per thread: online softmax in
+//   warps 3-6  softmax and epilogue, one row per thread: online softmax in
 //              the base-2 domain against a lazily moved reference maximum,
 //              P written back to TMEM as bf16; O and l are rescaled (in TMEM)
 //              only when a row's maximum grows by more than 2^8.
@@ -44,12 +47,11 @@
 namespace csa {
 
 namespace atc {
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
 constexpr int ROWS = 128;                 // MMA M
 constexpr int KT = 128;                   // keys per tile
 constexpr int D = 128;                    // head dim
 constexpr int ATOM = 128 * 128;           // 128 rows x 128 bytes (64 bf16 columns)
-constexpr int Q_BYTES = 2 * ATOM;
 constexpr int K_BYTES = 2 * ATOM;
 constexpr int V_BYTES = 2 * ATOM;
 constexpr int TMEM_COLS = 512;
@@ -58,36 +60,47 @@ constexpr int O_COL = 256;                // O accumulator at columns 256..383
 constexpr uint32_t IDESC_S = instr_desc(1u, 1u, ROWS, KT);          // bf16, both K-major
 constexpr uint32_t IDESC_PV = instr_desc(1u, 1u, ROWS, D, 0u, 1u);  // B (= V) MN-major
 constexpr uint32_t FULL = 0xFFFFFFFFu;
+constexpr int MAX_LIST = 4096;            // selected entries one CTA stages (sparse mode)
 
-template <int STAGES> struct Smem {
-    // barriers: q, mma_done, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full
-    static constexpr int N_BARS = 2 + 3 * STAGES + 5;
-    static constexpr int BYTES = 1024 + Q_BYTES + STAGES * (K_BYTES + V_BYTES) + N_BARS * 8 + STAGES * 16 + 16;
+// QROWS: Q rows loaded per CTA.  With 64 (one token of 64 heads) the two
+// 64-column Q blocks sit 8 KB apart; the MMA still reads 128 rows, and rows
+// 64..127 (which read neighbouring data) only feed unused accumulator lanes.
+template <int MODE, int STAGES, int QROWS> struct Cfg {
+    static constexpr int Q_ATOM = QROWS * 128;
+    static constexpr int Q_BYTES = 2 * Q_ATOM;
+    static constexpr int LIST = MODE == 0 ? MAX_LIST : 0;
+    // barriers: q, mma_done, list, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_full
+    static constexpr int N_BARS = 3 + 4 * STAGES + 5;
+    static constexpr int SMEM = 1024 + Q_BYTES + STAGES * (K_BYTES + V_BYTES) + LIST * 4 + N_BARS * 8 + 16;
+    static_assert(SMEM <= 232448, "shared memory");
 };
 }  // namespace atc
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int QROWS>
 __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v, const AttnTcParams p)
 {
     using namespace atc;
+    using C = Cfg<MODE, STAGES, QROWS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base;
-    uint8_t* sK = sQ + Q_BYTES;
+    uint8_t* sK = sQ + C::Q_BYTES;
     uint8_t* sV = sK + STAGES * K_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * V_BYTES);
+    int32_t* sidx = reinterpret_cast<int32_t*>(sV + STAGES * V_BYTES);   // sparse mode: the CTA's list
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sidx + C::LIST);
     uint64_t* bar_q = bars;
     uint64_t* bar_mma_done = bars + 1;
-    uint64_t* k_full = bars + 2;
+    uint64_t* bar_list = bars + 2;        // sparse mode: the staged list is complete
+    uint64_t* k_full = bars + 3;
     uint64_t* v_full = k_full + STAGES;
-    uint64_t* kv_empty = v_full + STAGES;
-    uint64_t* s_full = kv_empty + STAGES;
+    uint64_t* k_empty = v_full + STAGES;  // K stage free once S_j has completed
+    uint64_t* v_empty = k_empty + STAGES; // V stage free once P_j V_j has completed
+    uint64_t* s_full = v_empty + STAGES;
     uint64_t* p_full = s_full + 2;
     uint64_t* o_full = p_full + 2;        // one phase per completed P_j V_j
-    uint32_t* kmask = reinterpret_cast<uint32_t*>(bars + Smem<STAGES>::N_BARS);   // [STAGES][4]
-    uint32_t* tmem_holder = kmask + 4 * STAGES;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::N_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,10 +132,12 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
         mbar_init(bar_mma_done, 1);
+        mbar_init(bar_list, 1);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
@@ -132,7 +147,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 2) {
         tmem_alloc(tmem_holder, TMEM_COLS);
         tmem_relinquish();
     }
@@ -141,61 +156,81 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
-        if (n_tiles > 0) {
-            if (lane == 0) {
+    if (warp < 2) {
+        // ------------------------------ producers ------------------------------
+        const int pl = warp * 32 + lane;                     // 0..63
+        if (n_tiles > 0 && (MODE == 0 || warp == 0)) {
+            if (pl == 0) {
                 tma_prefetch_desc(&tmap_q);
-                tma_prefetch_desc(&tmap_k);
-                tma_prefetch_desc(&tmap_v);
+                if (MODE != 0) {
+                    tma_prefetch_desc(&tmap_k);
+                    tma_prefetch_desc(&tmap_v);
+                }
                 const int qrow = (b * p.n_q + i0) * p.H;
-                mbar_arrive_expect_tx(bar_q, Q_BYTES);
+                mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
                 tma_load_2d(sQ, &tmap_q, bar_q, 0, qrow);
-                tma_load_2d(sQ + ATOM, &tmap_q, bar_q, 64, qrow);
+                tma_load_2d(sQ + C::Q_ATOM, &tmap_q, bar_q, 64, qrow);
+            }
+            if constexpr (MODE == 0) {
+                // stage the CTA's slice of the selection list once (invalid -> -1),
+                // padded with -1 to whole tiles; eight loads in flight per lane
+                const int32_t* sel = p.topk + ((long long)b * p.n_q + i0) * p.k;
+                const int len = (int)(r_hi - r_lo), padded = n_tiles * KT;
+                for (int base0 = 0; base0 < padded; base0 += 64 * 8) {
+                    int v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = base0 + u * 64 + pl;
+                        v[u] = e < len ? __ldg(sel + r_lo + e) : -1;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = base0 + u * 64 + pl;
+                        if (e < padded) {
+                            int idx = v[u];
+                            if (idx >= p.N_kv || idx < -1) {
+                                flag_status(STATUS_BOUNDS);
+                                idx = -1;
+                            }
+                            sidx[e] = idx;
+                        }
+                    }
+                }
+                asm volatile("bar.sync 1, 64;" ::: "memory");
+                if (pl == 0) mbar_arrive(bar_list);
             }
             int issued = 0;
-            const int32_t* sel = (MODE == 0) ? p.topk + ((long long)b * p.n_q + i0) * p.k : nullptr;
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % STAGES;
+                const uint32_t par = ((j / STAGES) & 1) ^ 1;
                 int ok = 1;
-                if (lane == 0) ok = mbar_wait(&kv_empty[st], ((j / STAGES) & 1) ^ 1, abort_flag);
+                if (lane == 0) ok = mbar_wait(&k_empty[st], par, abort_flag);
                 if (!__shfl_sync(FULL, ok, 0)) break;
-                const long long pos0 = r_lo + (long long)j * KT;
                 if constexpr (MODE == 0) {
-                    int rows[4];
-                    uint32_t bal[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const long long pos = pos0 + 4 * lane + u;
-                        int idx = -1;
-                        if (pos < r_hi) idx = __ldg(sel + pos);
-                        if (idx >= p.N_kv || idx < -1) {
-                            flag_status(STATUS_BOUNDS);
-                            idx = -1;
-                        }
-                        const bool valid = idx >= 0;
-                        rows[u] = b * p.N_kv + (valid ? idx : 0);
-                        bal[u] = __ballot_sync(FULL, valid);
-                    }
-                    if (lane == 0) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) kmask[st * 4 + u] = bal[u];
-                        mbar_arrive_expect_tx(&k_full[st], K_BYTES);
-                        mbar_arrive_expect_tx(&v_full[st], V_BYTES);
-                    }
-                    __syncwarp();
-                    uint8_t* dk = sK + st * K_BYTES + lane * 512;
-                    uint8_t* dv = sV + st * V_BYTES + lane * 512;
-                    tma_gather4(dk, &tmap_k, &k_full[st], 0, rows[0], rows[1], rows[2], rows[3]);
-                    tma_gather4(dk + ATOM, &tmap_k, &k_full[st], 64, rows[0], rows[1], rows[2], rows[3]);
-                    tma_gather4(dv, &tmap_v, &v_full[st], 0, rows[0], rows[1], rows[2], rows[3]);
-                    tma_gather4(dv + ATOM, &tmap_v, &v_full[st], 64, rows[0], rows[1], rows[2], rows[3]);
+                    // 32 groups of 4 rows x 2 column blocks per tile: lane l of
+                    // warp w gathers rows 4l..4l+3, columns 64w..64w+63 (invalid
+                    // entries fetch row 0; the softmax masks them)
+                    const int4 q4 = reinterpret_cast<const int4*>(sidx + j * KT)[lane];
+                    const int bN = b * p.N_kv;
+                    const int r0 = bN + max(q4.x, 0), r1 = bN + max(q4.y, 0);
+                    const int r2 = bN + max(q4.z, 0), r3 = bN + max(q4.w, 0);
+                    const uint32_t off = (uint32_t)(warp * ATOM + lane * 512);
+                    if (pl == 0) mbar_arrive_expect_tx(&k_full[st], K_BYTES);
+                    tma_gather4(sK + st * K_BYTES + off, &tmap_k, &k_full[st], warp * 64, r0, r1, r2, r3);
+                    if (lane == 0) ok = mbar_wait(&v_empty[st], par, abort_flag);
+                    if (!__shfl_sync(FULL, ok, 0)) break;
+                    if (pl == 0) mbar_arrive_expect_tx(&v_full[st], V_BYTES);
+                    tma_gather4(sV + st * V_BYTES + off, &tmap_v, &v_full[st], warp * 64, r0, r1, r2, r3);
                 } else {
+                    const int krow = (int)((long long)b * p.N_kv + r_lo + (long long)j * KT);
                     if (lane == 0) {
-                        const int krow = (int)((long long)b * p.N_kv + pos0);
                         mbar_arrive_expect_tx(&k_full[st], K_BYTES);
                         tma_load_2d(sK + st * K_BYTES, &tmap_k, &k_full[st], 0, krow);
                         tma_load_2d(sK + st * K_BYTES + ATOM, &tmap_k, &k_full[st], 64, krow);
+                        ok = mbar_wait(&v_empty[st], par, abort_flag);
+                    }
+                    if (!__shfl_sync(FULL, ok, 0)) break;
+                    if (lane == 0) {
                         mbar_arrive_expect_tx(&v_full[st], V_BYTES);
                         tma_load_2d(sV + st * V_BYTES, &tmap_v, &v_full[st], 0, krow);
                         tma_load_2d(sV + st * V_BYTES + ATOM, &tmap_v, &v_full[st], 64, krow);
@@ -203,7 +238,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                 }
                 issued = j + 1;
             }
-            if (lane == 0 && *abort_flag) {
+            if (pl == 0 && *abort_flag) {
                 // let the copies already in flight land before the CTA exits
                 mbar_wait(bar_q, 0);
                 for (int j = max(0, issued - STAGES); j < issued; ++j) {
@@ -212,7 +247,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 2) {
         // --------------------------- MMA issuer ---------------------------
         if (lane == 0 && n_tiles > 0) {
             const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
@@ -229,7 +264,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                     const uint64_t b_desc = smem_desc(sVa + st * V_BYTES + ks * 2048, ATOM, 1024, SWZ_128B);
                     umma_f16_tmem_a(tmem + O_COL, a + ks * 8, b_desc, IDESC_PV, (i > 0 || ks > 0) ? 1u : 0u);
                 }
-                umma_commit(&kv_empty[st]);
+                umma_commit(&v_empty[st]);
                 umma_commit(o_full);
                 return true;
             };
@@ -245,11 +280,12 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const int atom = ks / 4;
                     const uint32_t koff = (ks % 4) * 32;
-                    const uint64_t a_desc = smem_desc(sQa + atom * ATOM + koff, 16, 1024, SWZ_128B);
+                    const uint64_t a_desc = smem_desc(sQa + atom * C::Q_ATOM + koff, 16, 1024, SWZ_128B);
                     const uint64_t b_desc = smem_desc(sKa + st * K_BYTES + atom * ATOM + koff, 16, 1024, SWZ_128B);
                     umma_f16(d, a_desc, b_desc, IDESC_S, ks > 0);
                 }
                 umma_commit(&s_full[sb]);
+                umma_commit(&k_empty[st]);
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
             if (ok) issue_pv(n_tiles - 1);
@@ -291,10 +327,10 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
 
         float m_ref = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % STAGES, sb = j & 1;
-            bool w = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag);
-            if (MODE == 0 && w) w = mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag);  // orders the mask
+        if (MODE == 0 && n_tiles > 0) ok = __all_sync(FULL, mbar_wait(bar_list, 0, abort_flag));
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const int sb = j & 1;
+            const bool w = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag);
             if (!__all_sync(FULL, w)) { ok = false; break; }
             tc_fence_after();
             if (!warp_idle) {
@@ -303,10 +339,13 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                 uint32_t mk[4] = {0u, 0u, 0u, 0u};
                 int lo_c = 0, hi_c = 0;
                 if (MODE == 0) {
-                    if (row_ok) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) mk[u] = kmask[st * 4 + u];
-                    }
+                    // bit l of word u: entry 4l + u of the tile is a valid index
+                    const int4 q4 = reinterpret_cast<const int4*>(sidx + j * KT)[lane];
+                    mk[0] = __ballot_sync(FULL, q4.x >= 0);
+                    mk[1] = __ballot_sync(FULL, q4.y >= 0);
+                    mk[2] = __ballot_sync(FULL, q4.z >= 0);
+                    mk[3] = __ballot_sync(FULL, q4.w >= 0);
+                    if (!row_ok) mk[0] = mk[1] = mk[2] = mk[3] = 0u;
                 } else {
                     const long long kbase = r_lo + (long long)j * KT;
                     const long long a = ka - kbase, e = kb - kbase;
@@ -318,13 +357,28 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
 #pragma unroll
                 for (int q = 0; q < KT / 32; ++q) tmem_ld32(s_addr + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
                 tmem_ld_wait();
-                float mx = -INFINITY;
+                // masked columns become -inf; a tile valid for every row of the
+                // warp (the common case) skips the masking
+                const bool full_row = (MODE == 0) ? (row_ok && (mk[0] & mk[1] & mk[2] & mk[3]) == FULL)
+                                                  : (lo_c == 0 && hi_c == KT);
+                if (!__all_sync(FULL, full_row)) {
 #pragma unroll
-                for (int c = 0; c < KT; ++c) {
-                    const bool v = (MODE == 0) ? ((mk[c & 3] >> (c >> 2)) & 1u) : (c >= lo_c && c < hi_c);
-                    sv[c] = v ? sv[c] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, sv[c]);
+                    for (int c = 0; c < KT; ++c) {
+                        const bool v = (MODE == 0) ? ((mk[c & 3] >> (c >> 2)) & 1u)
+                                                   : ((unsigned)(c - lo_c) < (unsigned)(hi_c - lo_c));
+                        sv[c] = v ? sv[c] : -INFINITY;
+                    }
                 }
+                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < KT; c += 8) {
+                    a0 = fmax3(a0, sv[c], sv[c + 1]);
+                    a1 = fmax3(a1, sv[c + 2], sv[c + 3]);
+                    a2 = fmax3(a2, sv[c + 4], sv[c + 5]);
+                    a3 = fmax3(a3, sv[c + 6], sv[c + 7]);
+                }
+                // scores are raw dot products; the positive scale commutes with max
+                const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
                 // move the reference maximum if this tile exceeds it by > 2^8
                 const bool move = mx > m_ref + RESCALE_LOG2;
                 const float m_new = move ? mx : m_ref;
@@ -355,8 +409,8 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                     uint32_t pk[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const float p0 = ex2_approx(sv[32 * q + 2 * u] + neg_m);
-                        const float p1 = ex2_approx(sv[32 * q + 2 * u + 1] + neg_m);
+                        const float p0 = ex2_approx(fmaf(sv[32 * q + 2 * u], sl2, neg_m));
+                        const float p1 = ex2_approx(fmaf(sv[32 * q + 2 * u + 1], sl2, neg_m));
                         sum += p0 + p1;
                         pk[u] = pack_bf16x2(p0, p1);
                     }
@@ -428,21 +482,27 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
-constexpr int ATTN_TC_STAGES = 2;
-
-size_t attn_tc_smem_bytes() { return atc::Smem<ATTN_TC_STAGES>::BYTES; }
-
 bool attn_tc_supported(int H, int D) { return (H == 64 || H == 128) && D == atc::D; }
 
 int attn_tc_tokens_per_cta(int mode, int H) { return mode == 0 ? 1 : atc::ROWS / H; }
 
-int attn_tc_box_rows(int mode) { return mode == 0 ? 1 : atc::KT; }
+int attn_tc_q_box_rows(int mode, int H) { return (mode == 0 && H == 64) ? 64 : 128; }
+
+template <int MODE, int STAGES, int QROWS>
+static void launch_one(dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const AttnTcParams& p, cudaStream_t s)
+{
+    auto kern = attn_tc_kernel<MODE, STAGES, QROWS>;
+    constexpr int smem = atc::Cfg<MODE, STAGES, QROWS>::SMEM;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+}
 
 cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const AttnTcParams& p, cudaStream_t s)
@@ -450,22 +510,15 @@ cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& t
     if ((long long)p.B * p.n_q == 0) return cudaSuccess;
     const int n_groups = (p.n_q + p.T - 1) / p.T;
     dim3 grid((unsigned)(n_groups * p.n_splits), (unsigned)p.B);
-    const int smem = (int)attn_tc_smem_bytes();
-    cudaError_t e;
     if (mode == 0) {
-        auto kern = attn_tc_kernel<0, ATTN_TC_STAGES>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+        if (p.H == 64) launch_one<0, 3, 64>(grid, tq, tk, tv, p, s);
+        else launch_one<0, 2, 128>(grid, tq, tk, tv, p, s);
     } else if (mode == 1) {
-        auto kern = attn_tc_kernel<1, ATTN_TC_STAGES>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+        launch_one<1, 3, 128>(grid, tq, tk, tv, p, s);
     } else {
-        auto kern = attn_tc_kernel<2, ATTN_TC_STAGES>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+        launch_one<2, 3, 128>(grid, tq, tk, tv, p, s);
     }
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.n_splits == 1) return e;
     AttnArgsT<__nv_bfloat16> a{};
     a.out = p.out;

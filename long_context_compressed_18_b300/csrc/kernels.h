@@ -67,8 +67,9 @@ cudaError_t launch_attn_simt(const AttnArgsT<TIO>& a, int H, int D, cudaStream_t
 cudaError_t launch_attn_combine(const AttnArgsT<__nv_bfloat16>& a, int H, int D, cudaStream_t s);
 
 // tcgen05 attention (BF16, D = 128, H in {64, 128}); tensor maps over
-// Q [B*n_q*H, 128], K / V [B*N_kv, 128], 64-column boxes with 128-byte swizzle
-// (Q box 128 rows; K / V box attn_tc_box_rows(mode) rows).
+// Q [B*n_q*H, 128] (box attn_tc_q_box_rows rows) and K / V [B*N_kv, 128]
+// (box 128 rows for the dense modes, 1 row for the sparse mode's gathers),
+// 64-column boxes with 128-byte swizzle.
 struct AttnTcParams {
     const int32_t* topk;   // [B, n_q, k] (mode 0)
     __nv_bfloat16* out;    // [B, n_q, H, 128]
@@ -83,7 +84,7 @@ struct AttnTcParams {
 };
 bool attn_tc_supported(int H, int D);
 int attn_tc_tokens_per_cta(int mode, int H);
-int attn_tc_box_rows(int mode);
+int attn_tc_q_box_rows(int mode, int H);
 cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const AttnTcParams& p, cudaStream_t s);
 

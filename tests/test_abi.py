@@ -51,6 +51,10 @@ def test_host_side_validation_without_gpu():
     assert st == 2
     st = L.hca_attn(1, 1, 0, 4, 8, 12, 128, 0.1, None, None, None, lib.BF16, None, None, None)
     assert st == 2
+    # the softmax scale must be positive and finite
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        st = L.hca_attn(1, 1, 0, 4, 8, 64, 128, bad, None, None, None, lib.BF16, None, None, None)
+        assert st == 1 and "scale" in L.csa_last_error().decode()
     # misaligned pointer
     st = L.swa_attn(1, 1, 0, 8, 4, 8, 64, 0.1, 8, 16, 16, lib.F32, 16, None, None)
     assert st == 3

@@ -119,6 +119,8 @@ SPARSE_CASES = [
     # 128 heads (every MMA row used); 2 splits of 256 positions, the second
     # ragged; the sets hold 225 visible entries, then -1 padding
     dict(B=2, n_q=3, q_pos0=900, m=4, N_c=226, k=300, H=128, d=128, dt="bf16"),
+    # eight 128-entry tiles per CTA (no split at n_q > 16): the gather ring wraps
+    dict(B=1, n_q=20, q_pos0=4 * 3000 - 20, m=4, N_c=3000, k=1024, H=64, d=128, dt="bf16"),
     # ragged last tile (k = 200) with early queries that see few or no entries
     dict(B=1, n_q=40, q_pos0=0, m=4, N_c=100, k=200, H=64, d=128, dt="bf16"),
     dict(B=1, n_q=100, q_pos0=0, m=4, N_c=256, k=64, H=8, d=64, dt="f32"),                  # short sets, -1 pads
