@@ -138,11 +138,12 @@ csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int
  * this library.
  *   Arguments and results as in csa_topk_select, without the workspace.
  *   Scratch: a fixed device array of CSA_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB)
- *   inside the library, enough for B * n_q * ceil(N_c / chunk) * k * 8 bytes
- *   of candidates (csa_topk_select_workspace_size reports the need) -- e.g.
- *   32 queries over 262,144 entries with k = 1024.  Larger selections return
- *   CSA_ERR_WORKSPACE and launch nothing.  Every GPU that loads the library
- *   holds the array until the process exits.
+ *   inside the library.  Rows longer than 32,768 entries need 8 * max(8192,
+ *   4k) bytes of it each, plus a few bytes (csa_topk_select_workspace_size
+ *   reports the need): with k = 1024, up to 63 such rows fit in one call --
+ *   e.g. 63 decode queries over 262,144 entries; shorter rows need none.  Larger selections return CSA_ERR_WORKSPACE and
+ *   launch nothing.  Every GPU that loads the library holds the array until
+ *   the process exits.
  *   The call allocates nothing.  Its first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) with that device current;
  *   make that first call before any stream capture.  All calls on a device

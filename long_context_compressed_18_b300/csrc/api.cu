@@ -299,10 +299,7 @@ static csa_status_t check_index_args(int B, int n_q, int64_t q_pos0, int m, int 
 
 static csa_status_t check_topk(int N_c, int k)
 {
-    if (k < 1 || k > 4096) return fail(CSA_ERR_UNSUPPORTED, "k=%d outside [1, 4096]", k);
-    TopkPlan p = topk_plan(N_c, k);
-    if (p.n_chunks > 1 && (long long)p.n_chunks * k > TOPK_MAX_MERGE)
-        return fail(CSA_ERR_UNSUPPORTED, "N_c=%d with k=%d exceeds the selection capacity", N_c, k);
+    if (!topk_supported(N_c, k)) return fail(CSA_ERR_UNSUPPORTED, "top-k needs 1 <= k <= 4096, N_c <= 524288 (k=%d, N_c=%d)", k, N_c);
     return CSA_OK;
 }
 

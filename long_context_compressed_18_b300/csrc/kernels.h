@@ -24,9 +24,10 @@ cudaError_t launch_compress(int B, int n, int m, int d, const float* logits, con
 
 // ---- top-k ----
 constexpr int TOPK_MAX_SINGLE = 32768;   // entries one CTA selects from (keys in smem)
-constexpr int TOPK_MAX_MERGE = 16384;    // candidates one CTA merges (keys + indices in smem)
+constexpr int TOPK_MAX_ROW = 524288;     // longest row (the select kernel's bitmaps)
 struct TopkPlan { int chunk; int n_chunks; };
 TopkPlan topk_plan(int N_c, int k);
+bool topk_supported(int N_c, int k);
 size_t topk_workspace_bytes(int rows, int N_c, int k);
 cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,

@@ -10,10 +10,8 @@
 // order -- i.e. ranking by (score desc, index asc).  No floating-point
 // atomics; the result does not depend on thread scheduling.
 //
-// Rows longer than one CTA's capacity are split: phase A selects the top-k of
-// each chunk (candidates keep ascending index order), phase B selects from
-// the concatenated candidates.  The global top-k is contained in the union of
-// the chunk top-k sets, so the result is identical to a single pass.
+// Rows longer than one CTA's capacity (TOPK_MAX_SINGLE) take the three
+// long-row kernels below.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -194,9 +192,8 @@ __device__ void load_score_keys(const float* __restrict__ src, int len, uint32_t
 
 // Ordered compaction: selected(e) = key > T || (key == T && eq-rank(e) < take_eq).
 // emit(pos, e) is called once per selected element with its output slot.
-template <typename Emit>
-__device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int take_eq,
-                                TopkShared& sh, Emit emit)
+template <typename Emit, typename Keys>
+__device__ void ordered_compact_by(Keys keyat, int len, uint32_t T, int take_eq, TopkShared& sh, Emit emit)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per = (((len + TOPK_WARPS - 1) / TOPK_WARPS) + 31) & ~31;
@@ -204,7 +201,7 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
     uint32_t n_take = 0, n_eq = 0;
     for (int e0 = lo; e0 < hi; e0 += 32) {
         const int e = e0 + lane;
-        const uint32_t key = e < hi ? keys[e] : 0u;
+        const uint32_t key = e < hi ? keyat(e) : 0u;
         n_take += __popc(__ballot_sync(0xFFFFFFFFu, e < hi && key > T));
         n_eq += __popc(__ballot_sync(0xFFFFFFFFu, e < hi && key == T));
     }
@@ -222,7 +219,7 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
     const unsigned lt = (1u << lane) - 1u;
     for (int e0 = lo; e0 < hi; e0 += 32) {
         const int e = e0 + lane;
-        const uint32_t key = e < hi ? keys[e] : 0u;
+        const uint32_t key = e < hi ? keyat(e) : 0u;
         const unsigned bgt = __ballot_sync(0xFFFFFFFFu, e < hi && key > T);
         const unsigned beq = __ballot_sync(0xFFFFFFFFu, e < hi && key == T);
         const uint32_t my_eq_rank = eq_base + __popc(beq & lt);
@@ -234,128 +231,412 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
     }
 }
 
-// MODE 0: fp32 score rows.  Each CTA handles chunk c of row r.  With
-//         n_chunks == 1 it writes the final indices (-1 padded); otherwise it
-//         writes min(k, chunk_len) candidates (key, index) for phase B.
-// MODE 1: phase B over the candidates of a row.  Every chunk but the last
-//         non-empty one contributes exactly k candidates, so a row's
-//         candidates are one contiguous run of its [n_chunks, k] buffer.
-template <int MODE>
+template <typename Emit>
+__device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int take_eq, TopkShared& sh, Emit emit)
+{
+    ordered_compact_by([&](int e) { return keys[e]; }, len, T, take_eq, sh, emit);
+}
+
+// Rows of at most TOPK_MAX_SINGLE entries: one CTA per row, keys staged in
+// shared memory; writes the final indices, -1 padded.
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc,
-    int k, int chunk, int n_chunks, uint32_t* cand_key, int32_t* cand_idx, int32_t* __restrict__ out,
-    long long out_b_stride)
+    int k, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
-    // phase A / single pass: one CTA per (row, chunk); phase B: one CTA per row
-    const int r = (MODE == 0) ? (int)(blockIdx.x / n_chunks) : (int)blockIdx.x;
-    const int c = (MODE == 0) ? (int)(blockIdx.x % n_chunks) : 0;
+    const int r = (int)blockIdx.x;
     const int i = r % n_q_rows;   // query index within the chunk of rows
     const long long out_row = (long long)(r / n_q_rows) * out_b_stride + i;
     long long nvl = (q_pos0 + i + 1) / m;
-    const int L = (int)(nvl < Nc ? nvl : Nc);
+    const int len = (int)(nvl < Nc ? nvl : Nc);
     const int tid = threadIdx.x;
+    const int kk = min(k, len);
+    int32_t* o = out + out_row * k;
+    for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
+    if (kk == 0) return;
+    if (len <= k) {
+        for (int e = tid; e < len; e += TOPK_THREADS) o[e] = e;
+        return;
+    }
     clear_hist(sh, 2048);
     __syncthreads();
+    load_score_keys(scores + (long long)r * ld, len, keys, sh);
+    __syncthreads();
+    uint32_t T;
+    int teq;
+    radix_threshold(keys, len, kk, sh, T, teq);
+    ordered_compact(keys, len, T, teq, sh, [&](int pos, int e) { if (pos < kk) o[pos] = e; });
+}
 
-    if constexpr (MODE == 0) {
-        const int c0 = c * chunk;
-        const int len = max(0, min(chunk, L - c0));
-        const float* row = scores + (long long)r * ld + c0;
-        const int kk = min(k, len);
-        if (n_chunks == 1) {
-            int32_t* o = out + out_row * k;
-            for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
-            if (kk == 0) return;
-            if (len <= k) {
-                for (int e = tid; e < len; e += TOPK_THREADS) o[e] = e;
-                return;
+// ---------------------------------------------------------------------------
+// Long rows (more than one CTA's capacity): three kernels.
+//   sample   one CTA per row: keys of 4096 evenly spaced entries; their key
+//            of rank ~2k * 4096 / L (plus a margin) becomes the row's
+//            collection threshold thr, expected to sit well below the k-th
+//            largest key;
+//   collect  one CTA per 16384-entry chunk: every entry with key >= thr is
+//            appended to the chunk's shared-memory list, whose slice of the
+//            row's entry list is then reserved with one global atomic;
+//   select   one CTA per row: if the row collected at least k entries (so
+//            the k-th largest key T is >= thr and every entry with key >= T
+//            was collected) and no more than the list holds, the exact
+//            threshold among the entries is found with the radix levels and
+//            the selected indices -- equal keys taken in index order -- are
+//            marked in a shared-memory bitmap and written in ascending
+//            order.  Otherwise (heavy ties, or a sample that misjudged the
+//            row) the row is selected by the same radix levels and ordered
+//            compaction streaming the row from global memory.
+// Both routes give the exact result; only their speed depends on the data.
+// ---------------------------------------------------------------------------
+constexpr int LR_CHUNK = 16384;
+constexpr int LR_SAMPLES = 4096;
+
+static int lr_cap(int k) { return k * 4 > 8192 ? k * 4 : 8192; }
+
+struct LongRowWs {
+    uint32_t* thr;    // [rows] collection threshold (a key)
+    uint32_t* cnt;    // [rows] entries collected (may exceed cap)
+    uint32_t* key;    // [rows][cap]
+    int32_t* idx;     // [rows][cap]
+    int cap;
+};
+
+static size_t lr_head_bytes(int rows) { return ((size_t)rows * 8 + 255) / 256 * 256; }
+
+static LongRowWs lr_ws(void* ws, int rows, int k)
+{
+    LongRowWs w;
+    uint8_t* p = reinterpret_cast<uint8_t*>(ws);
+    w.cap = lr_cap(k);
+    w.thr = reinterpret_cast<uint32_t*>(p);
+    w.cnt = w.thr + rows;
+    p += lr_head_bytes(rows);
+    w.key = reinterpret_cast<uint32_t*>(p);
+    p += (size_t)rows * w.cap * 4;
+    w.idx = reinterpret_cast<int32_t*>(p);
+    return w;
+}
+
+__device__ __forceinline__ int visible_len(long long q_pos0, int i, int m, int Nc)
+{
+    const long long nvl = (q_pos0 + i + 1) / m;
+    return (int)(nvl < Nc ? nvl : Nc);
+}
+
+// Streams score keys [c0, c0 + len) of a row: f(in_range, index, key) is
+// called the same number of times in every lane (callers use warp ballots).
+// 16-byte vector loads when the start is aligned, eight loads in flight.
+template <typename F>
+__device__ __forceinline__ void stream_keys(const float* __restrict__ row, int c0, int len, F f)
+{
+    constexpr int U = 8;
+    const int tid = threadIdx.x;
+    const float* src = row + c0;
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const int n4 = len >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        for (int base = 0; base < n4; base += TOPK_THREADS * U) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e4 = base + u * TOPK_THREADS + tid;
+                v[u] = e4 < n4 ? __ldg(s4 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            load_score_keys(row, len, keys, sh);
-            __syncthreads();
-            uint32_t T; int teq;
-            radix_threshold(keys, len, kk, sh, T, teq);
-            ordered_compact(keys, len, T, teq, sh, [&](int pos, int e) { if (pos < kk) o[pos] = e; });
-        } else {
-            uint32_t* ck = cand_key + ((long long)r * n_chunks + c) * k;
-            int32_t* ci = cand_idx + ((long long)r * n_chunks + c) * k;
-            if (kk == 0) return;
-            if (len <= k) {
-                for (int e = tid; e < len; e += TOPK_THREADS) { ck[e] = score_key(row[e]); ci[e] = c0 + e; }
-                return;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e4 = base + u * TOPK_THREADS + tid;
+                const bool in = e4 < n4;
+                const int e = c0 + 4 * e4;
+                f(in, e, score_key(v[u].x));
+                f(in, e + 1, score_key(v[u].y));
+                f(in, e + 2, score_key(v[u].z));
+                f(in, e + 3, score_key(v[u].w));
             }
-            load_score_keys(row, len, keys, sh);
-            __syncthreads();
-            uint32_t T; int teq;
-            radix_threshold(keys, len, kk, sh, T, teq);
-            ordered_compact(keys, len, T, teq, sh, [&](int pos, int e) {
-                if (pos < kk) { ck[pos] = keys[e]; ci[pos] = c0 + e; }
-            });
         }
-    } else {
-        int32_t* idxs = reinterpret_cast<int32_t*>(keys + (long long)n_chunks * k);
-        int total = 0;
-        for (int cc = 0; cc < n_chunks; ++cc) total += min(k, max(0, min(chunk, L - cc * chunk)));
-        const uint32_t* ck = cand_key + (long long)r * n_chunks * k;
-        const int32_t* ci = cand_idx + (long long)r * n_chunks * k;
-        constexpr int U = 8;
-        for (int base = 0; base < total; base += TOPK_THREADS * U) {
-            uint32_t kv[U];
-            int32_t iv[U];
+        done = 4 * n4;
+    }
+    for (int base = done; base < len; base += TOPK_THREADS * U) {
+        float v[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+        for (int u = 0; u < U; ++u) {
+            const int e = base + u * TOPK_THREADS + tid;
+            v[u] = e < len ? __ldg(src + e) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base + u * TOPK_THREADS + tid;
+            f(e < len, c0 + e, score_key(v[u]));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    LongRowWs w)
+{
+    __shared__ uint32_t keys[LR_SAMPLES];
+    __shared__ TopkShared sh;
+    const int r = blockIdx.x;
+    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
+    if (threadIdx.x == 0) w.cnt[r] = 0;
+    if (L <= k) return;                           // uniform: the row is copied whole
+    const int S = L < LR_SAMPLES ? L : LR_SAMPLES;
+    const float* row = scores + (long long)r * ld;
+    clear_hist(sh, 2048);
+    __syncthreads();
+    constexpr int U = LR_SAMPLES / TOPK_THREADS;
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int q = u * TOPK_THREADS + threadIdx.x;
+        v[u] = q < S ? __ldg(row + (int)((long long)q * L / S)) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int q = u * TOPK_THREADS + threadIdx.x;
+        if (q < S) {
+            const uint32_t key = score_key(v[u]);
+            keys[q] = key;
+            atomicAdd(&sh.hist[key >> 21], 1u);
+        }
+    }
+    __syncthreads();
+    // rank of the threshold among the samples: twice the expected rank of the
+    // k-th largest key, plus a margin of 8
+    long long want = 2ll * k * S / L + 8;
+    const int t_rank = (int)(want < S ? want : S);
+    uint32_t T;
+    int teq;
+    radix_threshold(keys, S, t_rank, sh, T, teq);
+    if (threadIdx.x == 0) w.thr[r] = T;
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    int n_chunks, LongRowWs w)
+{
+    // entries with key >= thr go to the chunk's shared-memory list; one
+    // global atomic then reserves the chunk's slice of the row's list (whose
+    // order does not matter to the select kernel)
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ uint32_t n_loc_s, base_s;
+    uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [cap]
+    int32_t* lidx = reinterpret_cast<int32_t*>(lkey + w.cap);
+    const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
+    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
+    if (L <= k) return;
+    const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
+    if (len == 0) return;
+    const uint32_t thr = __ldcg(w.thr + r);
+    if (threadIdx.x == 0) n_loc_s = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const uint32_t cap = (uint32_t)w.cap;
+    stream_keys(scores + (long long)r * ld, c0, len, [&](bool in, int e, uint32_t key) {
+        const bool take = in && key >= thr;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, take);
+        if (!bal) return;
+        uint32_t pos0 = 0;
+        if (lane == 0) pos0 = atomicAdd(&n_loc_s, (uint32_t)__popc(bal));
+        pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
+        if (take) {
+            const uint32_t pos = pos0 + __popc(bal & lt);
+            if (pos < cap) {
+                lkey[pos] = key;
+                lidx[pos] = e;
+            }
+        }
+    });
+    __syncthreads();
+    const uint32_t n_all = n_loc_s;
+    if (threadIdx.x == 0) base_s = atomicAdd(w.cnt + r, n_all);   // counts every entry, even past cap
+    __syncthreads();
+    const uint32_t base = base_s, n_loc = min(n_all, cap);
+    uint32_t* ek = w.key + (size_t)r * cap;
+    int32_t* ei = w.idx + (size_t)r * cap;
+    for (uint32_t q = threadIdx.x; q < n_loc; q += TOPK_THREADS) {
+        if (base + q < cap) {
+            ek[base + q] = lkey[q];
+            ei[base + q] = lidx[q];
+        }
+    }
+}
+
+// Block-wide exclusive prefix sum of one value per thread.
+__device__ uint32_t block_excl_scan(uint32_t v, TopkShared& sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    __syncthreads();
+    if (lane == 31) sh.scan[warp] = incl;
+    __syncthreads();
+    uint32_t before = incl - v;
+    for (int w = 0; w < warp; ++w) before += sh.scan[w];
+    return before;
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ TopkShared sh;
+    const int r = blockIdx.x;
+    const int i = r % n_q_rows;
+    int32_t* o = out + ((long long)(r / n_q_rows) * out_b_stride + i) * k;
+    const int L = visible_len(q_pos0, i, m, Nc);
+    const int kk = min(k, L);
+    const int tid = threadIdx.x;
+    for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
+    if (kk == 0) return;
+    if (L <= k) {
+        for (int e = tid; e < L; e += TOPK_THREADS) o[e] = e;
+        return;
+    }
+    const float* row = scores + (long long)r * ld;
+    const uint32_t got = __ldcg(w.cnt + r);
+    if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
+        // ---- the collected entries (every element with key >= thr) ----
+        const int nw = (L + 31) / 32;
+        uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw);   // [nw] bitmap of selected indices
+        uint32_t* eqm = sel + nw;                                 // [nw] bitmap of keys equal to T
+        uint32_t* ekey = eqm + nw;                                // [cap]
+        int32_t* eidx = reinterpret_cast<int32_t*>(ekey + w.cap);
+        const int n = (int)got;
+        clear_hist(sh, 2048);
+        for (int x = tid; x < 2 * nw; x += TOPK_THREADS) sel[x] = 0u;
+        __syncthreads();
+        for (int base = 0; base < n; base += TOPK_THREADS * 8) {
+            uint32_t kv[8];
+            int32_t iv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
                 const int e = base + u * TOPK_THREADS + tid;
-                kv[u] = e < total ? __ldg(ck + e) : 0u;
-                iv[u] = e < total ? __ldg(ci + e) : 0;
+                kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : 0u;
+                iv[u] = e < n ? __ldcg(w.idx + (size_t)r * w.cap + e) : 0;
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int e = base + u * TOPK_THREADS + tid;
-                if (e < total) {
-                    keys[e] = kv[u];
-                    idxs[e] = iv[u];
+                if (e < n) {
+                    ekey[e] = kv[u];
+                    eidx[e] = iv[u];
                     atomicAdd(&sh.hist[kv[u] >> 21], 1u);
                 }
             }
         }
         __syncthreads();
-        int32_t* o = out + out_row * k;
-        const int kk = min(k, total);
-        for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
-        if (kk == 0) return;
-        if (total <= k) {
-            for (int e = tid; e < total; e += TOPK_THREADS) o[e] = idxs[e];
-            return;
+        uint32_t T;
+        int teq;
+        radix_threshold(ekey, n, kk, sh, T, teq);
+        __syncthreads();
+        for (int e = tid; e < n; e += TOPK_THREADS) {
+            const uint32_t key = ekey[e];
+            const int j = eidx[e];
+            if (j < 0 || j >= L) continue;
+            if (key > T) atomicOr(&sel[j >> 5], 1u << (j & 31));
+            else if (key == T) atomicOr(&eqm[j >> 5], 1u << (j & 31));
         }
-        uint32_t T; int teq;
-        radix_threshold(keys, total, kk, sh, T, teq);
-        ordered_compact(keys, total, T, teq, sh, [&](int pos, int e) { if (pos < kk) o[pos] = idxs[e]; });
+        __syncthreads();
+        // equal keys: the first teq in index order join the selection
+        const int per = (nw + TOPK_THREADS - 1) / TOPK_THREADS;
+        const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
+        uint32_t ne = 0;
+        for (int x = w0; x < w1; ++x) ne += __popc(eqm[x]);
+        uint32_t rank = block_excl_scan(ne, sh);
+        for (int x = w0; x < w1; ++x) {
+            uint32_t bits = eqm[x];
+            if (!bits) continue;
+            const uint32_t nb = __popc(bits);
+            if (rank + nb <= (uint32_t)teq) {
+                sel[x] |= bits;
+            } else if (rank < (uint32_t)teq) {
+                for (uint32_t q = rank; q < (uint32_t)teq; ++q) {
+                    const uint32_t low = bits & (0u - bits);
+                    sel[x] |= low;
+                    bits ^= low;
+                }
+            }
+            rank += nb;
+        }
+        __syncthreads();
+        uint32_t ns = 0;
+        for (int x = w0; x < w1; ++x) ns += __popc(sel[x]);
+        uint32_t pos = block_excl_scan(ns, sh);
+        for (int x = w0; x < w1; ++x) {
+            uint32_t bits = sel[x];
+            while (bits) {
+                const int bpos = __ffs(bits) - 1;
+                if (pos < (uint32_t)kk) o[pos] = 32 * x + bpos;
+                ++pos;
+                bits &= bits - 1u;
+            }
+        }
+        return;
     }
+    // ---- heavy ties or a misjudged sample: stream the row from global memory ----
+    clear_hist(sh, 2048);
+    __syncthreads();
+    stream_keys(row, 0, L, [&](bool in, int, uint32_t key) {
+        if (in) atomicAdd(&sh.hist[key >> 21], 1u);
+    });
+    __syncthreads();
+    find_bin<2048>(sh, (uint32_t)kk);
+    const uint32_t b1 = sh.bin;
+    uint32_t rem = (uint32_t)kk - sh.above;
+    clear_hist(sh, 2048);
+    __syncthreads();
+    stream_keys(row, 0, L, [&](bool in, int, uint32_t key) {
+        if (in && (key >> 21) == b1) atomicAdd(&sh.hist[(key >> 10) & 0x7FFu], 1u);
+    });
+    __syncthreads();
+    find_bin<2048>(sh, rem);
+    const uint32_t pre = (b1 << 11) | sh.bin;
+    rem -= sh.above;
+    clear_hist(sh, 1024);
+    __syncthreads();
+    stream_keys(row, 0, L, [&](bool in, int, uint32_t key) {
+        if (in && (key >> 10) == pre) atomicAdd(&sh.hist[key & 0x3FFu], 1u);
+    });
+    __syncthreads();
+    find_bin<1024>(sh, rem);
+    const uint32_t T = (pre << 10) | sh.bin;
+    const int teq = (int)(rem - sh.above);
+    ordered_compact_by([&](int e) { return score_key(__ldg(row + e)); }, L, T, teq, sh,
+                       [&](int pos, int e) { if (pos < kk) o[pos] = e; });
 }
 
 // Chunking plan shared by the launcher and the workspace query.
 TopkPlan topk_plan(int N_c, int k)
 {
     TopkPlan p;
+    (void)k;
     if (N_c <= TOPK_MAX_SINGLE) {
         p.chunk = N_c > 0 ? N_c : 1;
         p.n_chunks = 1;
     } else {
-        int chunk = 16384;
-        while ((N_c + chunk - 1) / chunk * k > TOPK_MAX_MERGE && chunk < TOPK_MAX_SINGLE) chunk *= 2;
-        p.chunk = chunk;
-        p.n_chunks = (N_c + chunk - 1) / chunk;
+        p.chunk = LR_CHUNK;
+        p.n_chunks = (N_c + LR_CHUNK - 1) / LR_CHUNK;
     }
     return p;
 }
+
+bool topk_supported(int N_c, int k) { return k >= 1 && k <= 4096 && N_c >= 0 && N_c <= TOPK_MAX_ROW; }
 
 size_t topk_workspace_bytes(int rows, int N_c, int k)
 {
     TopkPlan p = topk_plan(N_c, k);
     if (p.n_chunks == 1) return 0;
-    return (size_t)rows * p.n_chunks * k * (sizeof(uint32_t) + sizeof(int32_t));
+    return lr_head_bytes(rows) + (size_t)rows * lr_cap(k) * 8;
 }
 
 cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
@@ -367,30 +648,24 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
     TopkPlan p = topk_plan(N_c, k);
     if (p.n_chunks == 1) {
         size_t smem = (size_t)p.chunk * sizeof(uint32_t);
-        auto kern = topk_kernel<0>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, p.chunk, 1,
-                                              nullptr, nullptr, out, out_b_stride);
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        topk_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
         return cudaGetLastError();
     }
-    uint32_t* ck = reinterpret_cast<uint32_t*>(ws);
-    int32_t* ci = reinterpret_cast<int32_t*>(ck + (size_t)rows * p.n_chunks * k);
-    {
-        size_t smem = (size_t)p.chunk * sizeof(uint32_t);
-        auto kern = topk_kernel<0>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<rows * p.n_chunks, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
-                                                           p.chunk, p.n_chunks, ck, ci, out, out_b_stride);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    {
-        size_t smem = (size_t)p.n_chunks * k * (sizeof(uint32_t) + sizeof(int32_t));
-        auto kern = topk_kernel<1>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, p.chunk,
-                                              p.n_chunks, ck, ci, out, out_b_stride);
-    }
+    const LongRowWs w = lr_ws(ws, rows, k);
+    topk_lr_sample_kernel<<<rows, TOPK_THREADS, 0, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w);
+    const size_t csmem = (size_t)w.cap * 8;
+    cudaFuncSetAttribute(topk_lr_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+    topk_lr_collect_kernel<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
+                                                                          p.n_chunks, w);
+    // the fast route needs two bitmaps of the row and the entry list in
+    // shared memory; shapes beyond that stream every row instead
+    size_t smem = (size_t)2 * ((N_c + 31) / 32) * 4 + (size_t)w.cap * 8;
+    const int fast_ok = smem <= (size_t)200 * 1024;
+    if (!fast_ok) smem = 0;
+    cudaFuncSetAttribute(topk_lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    topk_lr_select_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok,
+                                                          out, out_b_stride);
     return cudaGetLastError();
 }
 

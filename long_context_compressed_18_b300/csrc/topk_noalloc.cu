@@ -15,8 +15,9 @@
 
 namespace {
 
-// Scratch shared by every call on a device.  Sized for the 1M-context decode
-// shape: 32 rows x 16 chunks x 1024 candidates x (4-byte key + 4-byte index).
+// Scratch shared by every call on a device: for rows longer than one CTA's
+// capacity, a threshold, a counter and an entry list per row (64 KB a row at
+// k = 1024, so 63 rows of the 1M-context decode shape fit in 4 MiB).
 static __device__ __align__(256) uint8_t g_topk_scratch[CSA_TOPK_NOALLOC_SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
@@ -50,10 +51,7 @@ extern "C" csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, 
                                                 const float* scores, int32_t* topk, csa_stream_t stream)
 {
     if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || q_pos0 < 0) return csa::report(CSA_ERR_INVALID_ARG, "bad sizes");
-    if (k < 1 || k > 4096) return csa::report(CSA_ERR_UNSUPPORTED, "k outside [1, 4096]");
-    const csa::TopkPlan plan = csa::topk_plan(N_c, k);
-    if (plan.n_chunks > 1 && (long long)plan.n_chunks * k > csa::TOPK_MAX_MERGE)
-        return csa::report(CSA_ERR_UNSUPPORTED, "N_c with this k exceeds the selection capacity");
+    if (!csa::topk_supported(N_c, k)) return csa::report(CSA_ERR_UNSUPPORTED, "top-k needs 1 <= k <= 4096, N_c <= 524288");
     if ((long long)B * n_q == 0) return CSA_OK;
     if (!topk || (reinterpret_cast<uintptr_t>(topk) & 15u) ||
         (N_c > 0 && (!scores || (reinterpret_cast<uintptr_t>(scores) & 15u))))
@@ -68,8 +66,8 @@ extern "C" csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, 
         const csa_status_t st = scratch_address(&scratch);
         if (st != CSA_OK) return st;
     }
-    // Nothing in the scratch has to start at zero: within one call, phase A
-    // writes every candidate slot that phase B then reads.
+    // The per-row counters must start at zero: the first long-row kernel of
+    // launch_topk clears them on the stream before they are used.
     const cudaError_t e = csa::launch_topk(scores, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, scratch,
                                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return csa::report(CSA_ERR_CUDA, cudaGetErrorString(e));

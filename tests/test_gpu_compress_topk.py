@@ -104,8 +104,12 @@ def test_quantised_compression_within_format_error():
 
 # ---- top-k on identical scores: bit-exact --------------------------------
 
-def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed):
+def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed, order=None):
     sc = inputs.random_scores(B * n_q, Nc, seed=seed, tie_levels=tie_levels)
+    if order == "ascending":     # the best entries cluster at the end of the row
+        sc = sc.sort(dim=1).values.contiguous()
+    elif order == "descending":  # ... or at its start
+        sc = sc.sort(dim=1, descending=True).values.contiguous()
     out = torch.empty(B * n_q, k, dtype=torch.int32, device=DEV)
     ws_bytes = lib.csa_topk_select_workspace_size(B, n_q, Nc, k)
     ws = lib.empty_workspace(ws_bytes)
@@ -128,6 +132,17 @@ def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed):
     dict(B=3, n_q=1, q_pos0=(1 << 20) - 1, m=4, Nc=262144, k=1024, tie_levels=0),   # decode rows
     dict(B=2, n_q=1, q_pos0=(1 << 20) - 1, m=4, Nc=262144, k=1024, tie_levels=50),
     dict(B=1, n_q=3, q_pos0=2000, m=1, Nc=2003, k=4096, tie_levels=0),      # k > row length
+    dict(B=2, n_q=1, q_pos0=(1 << 20) - 1, m=4, Nc=262144, k=1024, tie_levels=1),   # threshold bin overflows
+    dict(B=1, n_q=4, q_pos0=4 * 33000 - 3, m=4, Nc=33000, k=4096, tie_levels=0),  # just past one CTA
+    dict(B=1, n_q=3, q_pos0=4 * 40001 - 3, m=4, Nc=40001, k=1000, tie_levels=0),  # odd row pitch, ragged tail
+    dict(B=1, n_q=2, q_pos0=4 * 524288 - 2, m=4, Nc=524288, k=2000, tie_levels=0),  # longest row
+    dict(B=1, n_q=2, q_pos0=4 * 524288 - 2, m=4, Nc=524288, k=4096, tie_levels=0),  # streamed route only
 ])
 def test_topk_bit_exact(case):
     _topk_case(seed=sum(case.values()) % 1000, **case)
+
+
+@pytest.mark.parametrize("order", ["ascending", "descending"])
+def test_topk_clustered_rows(order):
+    """Rows whose best entries sit together (in the last or first chunk)."""
+    _topk_case(B=2, n_q=1, q_pos0=(1 << 20) - 1, m=4, Nc=262144, k=1024, tie_levels=0, seed=77, order=order)

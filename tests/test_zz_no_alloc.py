@@ -52,10 +52,11 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
 
 
 def test_noalloc_rejects_selection_larger_than_scratch():
-    # 33 rows of 262,144 entries need 33 * 16 * 1024 * 8 bytes > 4 MiB
-    assert lib.csa_topk_select_workspace_size(33, 1, 262144, 1024) > lib.NOALLOC_SCRATCH_BYTES
-    sc = torch.zeros(33, 262144, dtype=torch.float32, device=DEV)
-    out = torch.empty(33, 1024, dtype=torch.int32, device=DEV)
+    # 63 rows of 262,144 entries fit the 4 MiB array; 64 do not
+    assert lib.csa_topk_select_workspace_size(63, 1, 262144, 1024) <= lib.NOALLOC_SCRATCH_BYTES
+    assert lib.csa_topk_select_workspace_size(64, 1, 262144, 1024) > lib.NOALLOC_SCRATCH_BYTES
+    sc = torch.zeros(64, 262144, dtype=torch.float32, device=DEV)
+    out = torch.empty(64, 1024, dtype=torch.int32, device=DEV)
     with pytest.raises(lib.CsaError) as e:
-        lib.csa_topk_select_noalloc(33, 1, (1 << 20) - 1, 4, 262144, 1024, sc, out)
+        lib.csa_topk_select_noalloc(64, 1, (1 << 20) - 1, 4, 262144, 1024, sc, out)
     assert e.value.status == 4 and "4 MiB" in str(e.value)
