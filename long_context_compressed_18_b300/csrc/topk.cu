@@ -89,7 +89,7 @@ __device__ void find_bin(TopkShared& sh, uint32_t rem)
 // are selected (take_eq), for 1 <= kk <= len.  Requires sh.hist to hold the
 // first-level histogram (key >> 21) of keys[0..len).
 __device__ void radix_threshold(const uint32_t* keys, int len, int kk, TopkShared& sh, uint32_t& T_out,
-                                int& take_eq_out)
+                                int& take_eq_out, uint32_t* n_eq_out = nullptr)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     find_bin<2048>(sh, (uint32_t)kk);
@@ -132,6 +132,7 @@ __device__ void radix_threshold(const uint32_t* keys, int len, int kk, TopkShare
     find_bin<1024>(sh, rem);
     T_out = (pre << 10) | sh.bin;
     take_eq_out = (int)(rem - sh.above);
+    if (n_eq_out) *n_eq_out = sh.hist[sh.bin];   // keys equal to T
 }
 
 // Loads len fp32 scores into shared memory as keys and accumulates the
@@ -383,7 +384,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
     const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
     if (threadIdx.x == 0) w.cnt[r] = 0;
     if (L <= k) return;                           // uniform: the row is copied whole
+    // 128 runs of 32 consecutive entries, evenly spaced (whole cache lines)
     const int S = L < LR_SAMPLES ? L : LR_SAMPLES;
+    const int runs = S / 32 > 0 ? S / 32 : 1;
     const float* row = scores + (long long)r * ld;
     clear_hist(sh, 2048);
     __syncthreads();
@@ -392,7 +395,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int q = u * TOPK_THREADS + threadIdx.x;
-        v[u] = q < S ? __ldg(row + (int)((long long)q * L / S)) : 0.f;
+        const int run = q >> 5;
+        const int e = (L < LR_SAMPLES) ? q : (int)((long long)run * (L - 32) / (runs > 1 ? runs - 1 : 1)) + (q & 31);
+        v[u] = q < S ? __ldg(row + e) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -414,13 +419,21 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
     if (threadIdx.x == 0) w.thr[r] = T;
 }
 
+// The float whose key is k (inverse of score_key on keys of non-NaN values).
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
     int n_chunks, LongRowWs w)
 {
-    // entries with key >= thr go to the chunk's shared-memory list; one
-    // global atomic then reserves the chunk's slice of the row's list (whose
-    // order does not matter to the select kernel)
+    // Entries with key >= thr go to the chunk's shared-memory list, then one
+    // global atomic reserves the chunk's slice of the row's list (whose order
+    // does not matter to the select kernel).  key >= thr is tested as the
+    // float comparison s >= value(thr), which orders -0 with +0 and never
+    // takes a NaN, exactly like the keys; a threshold key of 0 takes all.
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t n_loc_s, base_s;
     uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [cap]
@@ -431,26 +444,87 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
     if (len == 0) return;
     const uint32_t thr = __ldcg(w.thr + r);
+    const bool take_all = thr == 0u;
+    const float tf = key_value(thr);
     if (threadIdx.x == 0) n_loc_s = 0;
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const unsigned lt = (1u << lane) - 1u;
+    const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t cap = (uint32_t)w.cap;
-    stream_keys(scores + (long long)r * ld, c0, len, [&](bool in, int e, uint32_t key) {
-        const bool take = in && key >= thr;
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, take);
-        if (!bal) return;
-        uint32_t pos0 = 0;
-        if (lane == 0) pos0 = atomicAdd(&n_loc_s, (uint32_t)__popc(bal));
-        pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
-        if (take) {
-            const uint32_t pos = pos0 + __popc(bal & lt);
-            if (pos < cap) {
-                lkey[pos] = key;
-                lidx[pos] = e;
+    const float* src = scores + (long long)r * ld + c0;
+    // reserve warp slots for n entries of this lane; returns the lane's first slot
+    auto reserve = [&](uint32_t n) -> uint32_t {
+        uint32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t wb = 0;
+        if (lane == 31 && tot) wb = atomicAdd(&n_loc_s, tot);
+        wb = __shfl_sync(0xFFFFFFFFu, wb, 31);
+        return wb + incl - n;
+    };
+    auto put = [&](uint32_t& pos, float v, int e) {
+        if (pos < cap) {
+            lkey[pos] = score_key(v);
+            lidx[pos] = c0 + e;
+        }
+        ++pos;
+    };
+    constexpr int U = 8;
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+        const int n4 = len >> 2;
+        for (int base = 0; base < n4; base += TOPK_THREADS * U) {
+            float4 f[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e4 = base + u * TOPK_THREADS + tid;
+                f[u] = e4 < n4 ? __ldg(reinterpret_cast<const float4*>(src) + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            uint32_t mask = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (base + u * TOPK_THREADS + tid < n4) {
+                    mask |= (uint32_t)(take_all || f[u].x >= tf) << (4 * u);
+                    mask |= (uint32_t)(take_all || f[u].y >= tf) << (4 * u + 1);
+                    mask |= (uint32_t)(take_all || f[u].z >= tf) << (4 * u + 2);
+                    mask |= (uint32_t)(take_all || f[u].w >= tf) << (4 * u + 3);
+                }
+            }
+            if (!__any_sync(0xFFFFFFFFu, mask != 0u)) continue;
+            uint32_t pos = reserve(__popc(mask));
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (mask & (0xFu << (4 * u))) {
+                    const int e = 4 * (base + u * TOPK_THREADS + tid);
+                    if (mask >> (4 * u) & 1u) put(pos, f[u].x, e);
+                    if (mask >> (4 * u + 1) & 1u) put(pos, f[u].y, e + 1);
+                    if (mask >> (4 * u + 2) & 1u) put(pos, f[u].z, e + 2);
+                    if (mask >> (4 * u + 3) & 1u) put(pos, f[u].w, e + 3);
+                }
             }
         }
-    });
+        done = 4 * n4;
+    }
+    for (int base = done; base < len; base += TOPK_THREADS * U) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base + u * TOPK_THREADS + tid;
+            v[u] = e < len ? __ldg(src + e) : 0.f;
+        }
+        uint32_t mask = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * TOPK_THREADS + tid < len) mask |= (uint32_t)(take_all || v[u] >= tf) << u;
+        if (!__any_sync(0xFFFFFFFFu, mask != 0u)) continue;
+        uint32_t pos = reserve(__popc(mask));
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (mask >> u & 1u) put(pos, v[u], base + u * TOPK_THREADS + tid);
+    }
     __syncthreads();
     const uint32_t n_all = n_loc_s;
     if (threadIdx.x == 0) base_s = atomicAdd(w.cnt + r, n_all);   // counts every entry, even past cap
@@ -515,13 +589,15 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
         clear_hist(sh, 2048);
         for (int x = tid; x < 2 * nw; x += TOPK_THREADS) sel[x] = 0u;
         __syncthreads();
+        const uint32_t thr = __ldcg(w.thr + r);
+        uint32_t span = 0;     // max over entries of key - thr (every entry has key >= thr)
         for (int base = 0; base < n; base += TOPK_THREADS * 8) {
             uint32_t kv[8];
             int32_t iv[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int e = base + u * TOPK_THREADS + tid;
-                kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : 0u;
+                kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : thr;
                 iv[u] = e < n ? __ldcg(w.idx + (size_t)r * w.cap + e) : 0;
             }
 #pragma unroll
@@ -530,55 +606,104 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
                 if (e < n) {
                     ekey[e] = kv[u];
                     eidx[e] = iv[u];
-                    atomicAdd(&sh.hist[kv[u] >> 21], 1u);
+                    span = max(span, kv[u] - thr);
                 }
             }
         }
+        // The entries crowd into one or two first-level bins of the raw keys;
+        // rank them instead by (key - thr) << s, s putting the top bit of the
+        // span at bit 31 -- strictly increasing in key, so the threshold and
+        // the ties (and hence the selection) are the same, and the first
+        // radix level spreads over all its bins.
+#pragma unroll
+        for (int dd = 16; dd > 0; dd >>= 1) span = max(span, __shfl_xor_sync(0xFFFFFFFFu, span, dd));
+        if ((tid & 31) == 0) sh.scan[tid >> 5] = span;
         __syncthreads();
-        uint32_t T;
+        span = 0;
+        for (int q = 0; q < TOPK_WARPS; ++q) span = max(span, sh.scan[q]);
+        const int shl = span ? __clz(span) : 0;
+        for (int e = tid; e < n; e += TOPK_THREADS) {
+            const uint32_t tk = (ekey[e] - thr) << shl;
+            ekey[e] = tk;
+            atomicAdd(&sh.hist[tk >> 21], 1u);
+        }
+        __syncthreads();
+        uint32_t T, n_eq;
         int teq;
-        radix_threshold(ekey, n, kk, sh, T, teq);
+        radix_threshold(ekey, n, kk, sh, T, teq, &n_eq);
         __syncthreads();
+        // mark the selection; keys equal to T join it directly unless only some
+        // of them are taken (then the first teq in index order, below)
+        const bool all_eq = n_eq == (uint32_t)teq;
         for (int e = tid; e < n; e += TOPK_THREADS) {
             const uint32_t key = ekey[e];
             const int j = eidx[e];
             if (j < 0 || j >= L) continue;
-            if (key > T) atomicOr(&sel[j >> 5], 1u << (j & 31));
+            if (key > T || (key == T && all_eq)) atomicOr(&sel[j >> 5], 1u << (j & 31));
             else if (key == T) atomicOr(&eqm[j >> 5], 1u << (j & 31));
         }
         __syncthreads();
-        // equal keys: the first teq in index order join the selection
-        const int per = (nw + TOPK_THREADS - 1) / TOPK_THREADS;
-        const int w0 = min(nw, tid * per), w1 = min(nw, w0 + per);
-        uint32_t ne = 0;
-        for (int x = w0; x < w1; ++x) ne += __popc(eqm[x]);
-        uint32_t rank = block_excl_scan(ne, sh);
-        for (int x = w0; x < w1; ++x) {
-            uint32_t bits = eqm[x];
-            if (!bits) continue;
-            const uint32_t nb = __popc(bits);
-            if (rank + nb <= (uint32_t)teq) {
-                sel[x] |= bits;
-            } else if (rank < (uint32_t)teq) {
-                for (uint32_t q = rank; q < (uint32_t)teq; ++q) {
-                    const uint32_t low = bits & (0u - bits);
-                    sel[x] |= low;
-                    bits ^= low;
+        const int lane = tid & 31, warp = tid >> 5;
+        if (!all_eq) {
+            // warp-cooperative walk of the tie bitmap: warp w owns words [wa, wb)
+            const int per_w = ((nw + TOPK_WARPS - 1) / TOPK_WARPS + 31) & ~31;
+            const int wa = min(nw, warp * per_w), wb = min(nw, wa + per_w);
+            uint32_t t = 0;
+            for (int x = wa + lane; x < wb; x += 32) t += __popc(eqm[x]);
+#pragma unroll
+            for (int dd = 16; dd > 0; dd >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, dd);
+            if (lane == 0) sh.scan[warp] = t;
+            __syncthreads();
+            uint32_t rank = 0;
+            for (int q = 0; q < warp; ++q) rank += sh.scan[q];
+            for (int x0 = wa; x0 < wb; x0 += 32) {
+                const int x = x0 + lane;
+                uint32_t bits = x < wb ? eqm[x] : 0u;
+                const uint32_t nb = __popc(bits);
+                uint32_t incl = nb;
+#pragma unroll
+                for (int dd = 1; dd < 32; dd <<= 1) {
+                    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, dd);
+                    if (lane >= dd) incl += v;
                 }
+                const uint32_t r0 = rank + incl - nb;
+                if (bits) {
+                    if (r0 + nb <= (uint32_t)teq) {
+                        sel[x] |= bits;
+                    } else if (r0 < (uint32_t)teq) {
+                        for (uint32_t q = r0; q < (uint32_t)teq; ++q) {
+                            const uint32_t low = bits & (0u - bits);
+                            sel[x] |= low;
+                            bits ^= low;
+                        }
+                    }
+                }
+                rank += __shfl_sync(0xFFFFFFFFu, incl, 31);
             }
-            rank += nb;
+            __syncthreads();
+        }
+        // output slot of index j: (selected indices in words before j's) +
+        // (selected bits below j in its word); the per-word prefix goes into
+        // the tie bitmap's storage
+        uint32_t* wpre = eqm;
+        const int per_t = (nw + TOPK_THREADS - 1) / TOPK_THREADS;
+        const int t0 = min(nw, tid * per_t), t1 = min(nw, t0 + per_t);
+        uint32_t cntw = 0;
+        for (int x = t0; x < t1; ++x) cntw += __popc(sel[x]);
+        uint32_t run = block_excl_scan(cntw, sh);
+        for (int x = t0; x < t1; ++x) {
+            const uint32_t c = __popc(sel[x]);
+            wpre[x] = run;
+            run += c;
         }
         __syncthreads();
-        uint32_t ns = 0;
-        for (int x = w0; x < w1; ++x) ns += __popc(sel[x]);
-        uint32_t pos = block_excl_scan(ns, sh);
-        for (int x = w0; x < w1; ++x) {
-            uint32_t bits = sel[x];
-            while (bits) {
-                const int bpos = __ffs(bits) - 1;
-                if (pos < (uint32_t)kk) o[pos] = 32 * x + bpos;
-                ++pos;
-                bits &= bits - 1u;
+        for (int e = tid; e < n; e += TOPK_THREADS) {
+            const int j = eidx[e];
+            if (j < 0 || j >= L) continue;
+            const uint32_t word = sel[j >> 5], bit = 1u << (j & 31);
+            if (word & bit) {
+                const uint32_t pos = wpre[j >> 5] + __popc(word & (bit - 1u));
+                if (pos < (uint32_t)kk) o[pos] = j;
             }
         }
         return;
