@@ -253,6 +253,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Paired fp32 arithmetic (sm_100+): two IEEE fp32 FMAs, round to nearest,
+// in one instruction on a 64-bit register pair (x in the low half).
+__device__ __forceinline__ uint64_t pack_f32x2(float x, float y)
+{
+    return (uint64_t)__float_as_uint(x) | ((uint64_t)__float_as_uint(y) << 32);
+}
+__device__ __forceinline__ uint64_t pack_u32x2(uint32_t x, uint32_t y) { return (uint64_t)x | ((uint64_t)y << 32); }
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v)
+{
+    return make_float2(__uint_as_float((uint32_t)v), __uint_as_float((uint32_t)(v >> 32)));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // max(a, b, c) in one instruction (sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {

@@ -25,7 +25,11 @@
 namespace csa {
 
 namespace idx {
-constexpr int THREADS = 192;
+// warps 0-1 producer and MMA issuer, then EPI_WARPS epilogue warps: 4 for one
+// token per group (decode), 8 for four tokens (two per warp, two warps per
+// TMEM lane quadrant)
+template <int T> constexpr int epi_warps() { return T == 1 ? 4 : 8; }
+template <int T> constexpr int threads() { return 64 + 32 * epi_warps<T>(); }
 constexpr int BLOCK_KEYS = 128;   // MMA M
 constexpr int HEADS = 64;         // indexer heads
 constexpr int DIM = 128;          // indexer head dim
@@ -53,8 +57,38 @@ template <bool FP8, int T> struct Cfg {
 };
 }  // namespace idx
 
+// Score of one (key, token): the head sum sum_h sq[h] * acc[h] over the 64
+// accumulator columns (lo = heads 0-31, hi = heads 32-63) with paired FMAs,
+// times the key scale; stored if the key is visible to the token.
+__device__ __forceinline__ void idx_store_score(const uint32_t (&lo)[32], const uint32_t (&hi)[32],
+                                                const float* __restrict__ sq, float sk, int key, int tt, int i0,
+                                                int n_q_rows, long long tq, int m, int Nc, float* __restrict__ scores,
+                                                long long srow)
+{
+    const float4* sq4 = reinterpret_cast<const float4*>(sq);
+    uint64_t pa = 0, pb = 0;   // packed partial sums (x, y halves)
+#pragma unroll
+    for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 w4 = sq4[h4];
+        pa = ffma2(pack_f32x2(w4.x, w4.y), pack_u32x2(lo[4 * h4], lo[4 * h4 + 1]), pa);
+        pb = ffma2(pack_f32x2(w4.z, w4.w), pack_u32x2(lo[4 * h4 + 2], lo[4 * h4 + 3]), pb);
+    }
+#pragma unroll
+    for (int h4 = 0; h4 < 8; ++h4) {
+        const float4 w4 = sq4[8 + h4];
+        pa = ffma2(pack_f32x2(w4.x, w4.y), pack_u32x2(hi[4 * h4], hi[4 * h4 + 1]), pa);
+        pb = ffma2(pack_f32x2(w4.z, w4.w), pack_u32x2(hi[4 * h4 + 2], hi[4 * h4 + 3]), pb);
+    }
+    const float2 fa = unpack_f32x2(pa), fb = unpack_f32x2(pb);
+    const float sc = ((fa.x + fa.y) + (fb.x + fb.y)) * sk;
+    if (i0 + tt < n_q_rows) {
+        const long long nvt = (tq + tt + 1) / m;
+        if (key < nvt && key < Nc) scores[(srow + tt) * Nc + key] = sc;
+    }
+}
+
 template <bool FP8, int T>
-__global__ void __launch_bounds__(idx::THREADS, 1) indexer_tc_kernel(
+__global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const float* __restrict__ q_scale, const float* __restrict__ k_scale, float* __restrict__ scores,
     int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int n_splits,
@@ -90,7 +124,10 @@ __global__ void __launch_bounds__(idx::THREADS, 1) indexer_tc_kernel(
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
-        for (int a = 0; a < C::ACC; ++a) { mbar_init(&bar_acc_full[a], 1); mbar_init(&bar_acc_empty[a], 4); }
+        for (int a = 0; a < C::ACC; ++a) {
+            mbar_init(&bar_acc_full[a], 1);
+            mbar_init(&bar_acc_empty[a], idx::epi_warps<T>());
+        }
         mbar_init(bar_q, 1);
         mbar_init(bar_mma_done, 1);
         *abort_flag = 0;
@@ -163,18 +200,25 @@ __global__ void __launch_bounds__(idx::THREADS, 1) indexer_tc_kernel(
             mbar_wait(bar_mma_done, 0);
         }
     } else {
-        // ---------------- epilogue: 4 warps, one TMEM lane (= key) per thread ----
+        // ---------------- epilogue: one TMEM lane (= key) per thread ----------------
+        // Warp w (w >= 2) reads lane quadrant w % 4; with T = 4 the two warps of
+        // a quadrant take tokens {0, 1} and {2, 3}.  All of a warp's columns
+        // for the tile are loaded before one wait; head sums use paired FMAs.
+        constexpr int EW = idx::epi_warps<T>();
+        constexpr int TPW = T == 1 ? 1 : 2;        // tokens per epilogue warp
         const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
-        const int et = threadIdx.x - 64;           // 0..127
-        for (int x = et; x < T * idx::HEADS; x += 128) {
+        const int ew = warp - 2;                   // 0..EW-1
+        const int tt0 = (ew / 4) * TPW;            // first token of this warp
+        const int et = threadIdx.x - 64;           // 0..32*EW-1
+        for (int x = et; x < T * idx::HEADS; x += 32 * EW) {
             const int tt = x / idx::HEADS, h = x % idx::HEADS;
             const int i = i0 + tt;
             float v = 0.f;
             if (i < n_q_rows) v = q_scale ? q_scale[((long long)b * n_q_total + i_start + i) * idx::HEADS + h] : 1.f;
             sq_s[x] = v;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
         for (int li = 0; li < n_tiles; ++li) {
             const int acc = li % C::ACC;
             const int key = (tile0 + li) * idx::BLOCK_KEYS + row;
@@ -182,40 +226,25 @@ __global__ void __launch_bounds__(idx::THREADS, 1) indexer_tc_kernel(
             const bool ok = mbar_wait(&bar_acc_full[acc], (li / C::ACC) & 1, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;   // tcgen05.ld below is warp-collective
             tc_fence_after();
-#pragma unroll 1
-            for (int tt = 0; tt < T; ++tt) {
-                uint32_t v0[32], v1[32];
-                const uint32_t taddr = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::N + tt * idx::HEADS;
-                tmem_ld32(taddr, v0);
-                tmem_ld32(taddr + 32, v1);
-                tmem_ld_wait();
-                const float* sq = sq_s + tt * idx::HEADS;
-                float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-                for (int h = 0; h < 32; h += 4) {
-                    p0 = fmaf(sq[h], __uint_as_float(v0[h]), p0);
-                    p1 = fmaf(sq[h + 1], __uint_as_float(v0[h + 1]), p1);
-                    p2 = fmaf(sq[h + 2], __uint_as_float(v0[h + 2]), p2);
-                    p3 = fmaf(sq[h + 3], __uint_as_float(v0[h + 3]), p3);
-                }
-#pragma unroll
-                for (int h = 0; h < 32; h += 4) {
-                    p0 = fmaf(sq[32 + h], __uint_as_float(v1[h]), p0);
-                    p1 = fmaf(sq[33 + h], __uint_as_float(v1[h + 1]), p1);
-                    p2 = fmaf(sq[34 + h], __uint_as_float(v1[h + 2]), p2);
-                    p3 = fmaf(sq[35 + h], __uint_as_float(v1[h + 3]), p3);
-                }
-                const float s = ((p0 + p1) + (p2 + p3)) * sk;
-                const int i = i0 + tt;
-                if (i < n_q_rows) {
-                    long long nvt = (q_pos0 + i_start + i + 1) / m;
-                    if (key < nvt && key < Nc)
-                        scores[((long long)b * n_q_rows + i) * Nc + key] = s;
-                }
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::N + tt0 * idx::HEADS;
+            uint32_t va[32], vb[32], vc[32], vd[32];   // token tt0: va|vb, token tt0+1: vc|vd
+            tmem_ld32(tbase, va);
+            tmem_ld32(tbase + 32, vb);
+            if constexpr (TPW == 2) {
+                tmem_ld32(tbase + idx::HEADS, vc);
+                tmem_ld32(tbase + idx::HEADS + 32, vd);
             }
+            tmem_ld_wait();
+            // the accumulator can be refilled once the registers hold it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_acc_empty[acc]);
+            const long long srow = (long long)b * n_q_rows + i0;
+            const long long tq = q_pos0 + i_start + i0;   // position of token 0 of the group
+            idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, tt0, i0, n_q_rows, tq, m, Nc, scores, srow);
+            if constexpr (TPW == 2)
+                idx_store_score(vc, vd, sq_s + (tt0 + 1) * idx::HEADS, sk, key, tt0 + 1, i0, n_q_rows, tq, m, Nc,
+                                scores, srow);
         }
     }
 
@@ -346,7 +375,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     auto kern = indexer_tc_kernel<FP8, T>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     dim3 grid(n_groups * splits, B);
-    kern<<<grid, idx::THREADS, C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, n_q_total, i_start, n_q_rows,
+    kern<<<grid, idx::threads<T>(), C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, n_q_total, i_start, n_q_rows,
                                              q_pos0, m, Nc, splits, split_tiles);
     return cudaGetLastError();
 }
