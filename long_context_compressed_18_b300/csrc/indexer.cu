@@ -12,10 +12,11 @@
 // per-thread reduction over 64 columns (no cross-lane traffic).  T = 4 tokens
 // (N = 256) for prefill, T = 1 (N = 64) for decode.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (the query group once,
-// then a ring of key tiles); warp 1 owns the TMEM allocation and issues the
-// MMAs from one thread; warps 2-5 drain TMEM (tcgen05.ld), apply the scales,
-// sum over heads and store fp32 scores.  Accumulators are multi-buffered in
+// Warp roles: warp 0 issues TMA loads (the query group once, then a ring of
+// key tiles); warp 1 owns the TMEM allocation and issues the MMAs from one
+// thread; 4 * T epilogue warps (one token each, four per TMEM lane quadrant
+// for T = 4) drain TMEM (tcgen05.ld), apply the scales, sum over heads and
+// store fp32 scores.  Accumulators are multi-buffered in
 // TMEM so the MMA of tile i+1 overlaps the epilogue of tile i.  Every mbarrier
 // wait is bounded; on a timeout the CTA drains its copies and MMAs, frees
 // TMEM and exits with the device status word set.
@@ -25,10 +26,10 @@
 namespace csa {
 
 namespace idx {
-// warps 0-1 producer and MMA issuer, then EPI_WARPS epilogue warps: 4 for one
-// token per group (decode), 8 for four tokens (two per warp, two warps per
-// TMEM lane quadrant)
-template <int T> constexpr int epi_warps() { return T == 1 ? 4 : 8; }
+// warps 0-1 producer and MMA issuer, then the epilogue warps, one token each:
+// 4 for one token per group (decode), 16 for four tokens (four warps per TMEM
+// lane quadrant, so each scheduler has four epilogue warps to switch between)
+template <int T> constexpr int epi_warps() { return 4 * T; }
 template <int T> constexpr int threads() { return 64 + 32 * epi_warps<T>(); }
 constexpr int BLOCK_KEYS = 128;   // MMA M
 constexpr int HEADS = 64;         // indexer heads
@@ -66,21 +67,18 @@ __device__ __forceinline__ void idx_store_score(const uint32_t (&lo)[32], const 
                                                 long long srow)
 {
     const float4* sq4 = reinterpret_cast<const float4*>(sq);
-    uint64_t pa = 0, pb = 0;   // packed partial sums (x, y halves)
+    uint64_t pa = 0, pb = 0, pc = 0, pd = 0;   // packed partial sums (x, y halves)
 #pragma unroll
     for (int h4 = 0; h4 < 8; ++h4) {
         const float4 w4 = sq4[h4];
+        const float4 u4 = sq4[8 + h4];
         pa = ffma2(pack_f32x2(w4.x, w4.y), pack_u32x2(lo[4 * h4], lo[4 * h4 + 1]), pa);
         pb = ffma2(pack_f32x2(w4.z, w4.w), pack_u32x2(lo[4 * h4 + 2], lo[4 * h4 + 3]), pb);
+        pc = ffma2(pack_f32x2(u4.x, u4.y), pack_u32x2(hi[4 * h4], hi[4 * h4 + 1]), pc);
+        pd = ffma2(pack_f32x2(u4.z, u4.w), pack_u32x2(hi[4 * h4 + 2], hi[4 * h4 + 3]), pd);
     }
-#pragma unroll
-    for (int h4 = 0; h4 < 8; ++h4) {
-        const float4 w4 = sq4[8 + h4];
-        pa = ffma2(pack_f32x2(w4.x, w4.y), pack_u32x2(hi[4 * h4], hi[4 * h4 + 1]), pa);
-        pb = ffma2(pack_f32x2(w4.z, w4.w), pack_u32x2(hi[4 * h4 + 2], hi[4 * h4 + 3]), pb);
-    }
-    const float2 fa = unpack_f32x2(pa), fb = unpack_f32x2(pb);
-    const float sc = ((fa.x + fa.y) + (fb.x + fb.y)) * sk;
+    const float2 fa = unpack_f32x2(pa), fb = unpack_f32x2(pb), fc = unpack_f32x2(pc), fd = unpack_f32x2(pd);
+    const float sc = (((fa.x + fa.y) + (fb.x + fb.y)) + ((fc.x + fc.y) + (fd.x + fd.y))) * sk;
     if (i0 + tt < n_q_rows) {
         const long long nvt = (tq + tt + 1) / m;
         if (key < nvt && key < Nc) scores[(srow + tt) * Nc + key] = sc;
@@ -201,11 +199,11 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
         }
     } else {
         // ---------------- epilogue: one TMEM lane (= key) per thread ----------------
-        // Warp w (w >= 2) reads lane quadrant w % 4; with T = 4 the two warps of
-        // a quadrant take tokens {0, 1} and {2, 3}.  All of a warp's columns
-        // for the tile are loaded before one wait; head sums use paired FMAs.
+        // Warp w (w >= 2) reads lane quadrant w % 4 and takes token (w - 2) / 4
+        // of the group.  Both halves of its 64 columns are loaded before one
+        // wait; the head sum uses paired FMAs in four independent chains.
         constexpr int EW = idx::epi_warps<T>();
-        constexpr int TPW = T == 1 ? 1 : 2;        // tokens per epilogue warp
+        constexpr int TPW = 1;                     // tokens per epilogue warp
         const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
         const int ew = warp - 2;                   // 0..EW-1
