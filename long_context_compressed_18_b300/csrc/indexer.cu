@@ -60,11 +60,11 @@ template <bool FP8, int T> struct Cfg {
 
 // Score of one (key, token): the head sum sum_h sq[h] * acc[h] over the 64
 // accumulator columns (lo = heads 0-31, hi = heads 32-63) with paired FMAs,
-// times the key scale; stored if the key is visible to the token.
+// times the key scale; stored if key < nv (the token's visible entries; -1
+// for a token past the end of the rows).
 __device__ __forceinline__ void idx_store_score(const uint32_t (&lo)[32], const uint32_t (&hi)[32],
-                                                const float* __restrict__ sq, float sk, int key, int tt, int i0,
-                                                int n_q_rows, long long tq, int m, int Nc, float* __restrict__ scores,
-                                                long long srow)
+                                                const float* __restrict__ sq, float sk, int key, int nv,
+                                                float* __restrict__ srow_ptr)
 {
     const float4* sq4 = reinterpret_cast<const float4*>(sq);
     uint64_t pa = 0, pb = 0, pc = 0, pd = 0;   // packed partial sums (x, y halves)
@@ -79,10 +79,7 @@ __device__ __forceinline__ void idx_store_score(const uint32_t (&lo)[32], const 
     }
     const float2 fa = unpack_f32x2(pa), fb = unpack_f32x2(pb), fc = unpack_f32x2(pc), fd = unpack_f32x2(pd);
     const float sc = (((fa.x + fa.y) + (fb.x + fb.y)) + ((fc.x + fc.y) + (fd.x + fd.y))) * sk;
-    if (i0 + tt < n_q_rows) {
-        const long long nvt = (tq + tt + 1) / m;
-        if (key < nvt && key < Nc) scores[(srow + tt) * Nc + key] = sc;
-    }
+    if (key < nv) srow_ptr[key] = sc;
 }
 
 template <bool FP8, int T>
@@ -203,11 +200,10 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
         // of the group.  Both halves of its 64 columns are loaded before one
         // wait; the head sum uses paired FMAs in four independent chains.
         constexpr int EW = idx::epi_warps<T>();
-        constexpr int TPW = 1;                     // tokens per epilogue warp
         const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
         const int row = quad * 32 + lane;
         const int ew = warp - 2;                   // 0..EW-1
-        const int tt0 = (ew / 4) * TPW;            // first token of this warp
+        const int tt0 = ew / 4;                    // this warp's token within the group
         const int et = threadIdx.x - 64;           // 0..32*EW-1
         for (int x = et; x < T * idx::HEADS; x += 32 * EW) {
             const int tt = x / idx::HEADS, h = x % idx::HEADS;
@@ -217,6 +213,14 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             sq_s[x] = v;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+        // this warp's token: visible entries (constant over the tiles) and score row
+        const int i_tok = i0 + tt0;
+        int nv_tok = -1;
+        if (i_tok < n_q_rows) {
+            const long long nvl_t = (q_pos0 + i_start + i_tok + 1) / m;
+            nv_tok = (int)(nvl_t < Nc ? nvl_t : Nc);
+        }
+        float* const srow_ptr = scores + ((long long)b * n_q_rows + (i_tok < n_q_rows ? i_tok : 0)) * Nc;
         for (int li = 0; li < n_tiles; ++li) {
             const int acc = li % C::ACC;
             const int key = (tile0 + li) * idx::BLOCK_KEYS + row;
@@ -225,24 +229,15 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             if (!__all_sync(0xFFFFFFFFu, ok)) break;   // tcgen05.ld below is warp-collective
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * C::N + tt0 * idx::HEADS;
-            uint32_t va[32], vb[32], vc[32], vd[32];   // token tt0: va|vb, token tt0+1: vc|vd
+            uint32_t va[32], vb[32];   // heads 0-31 | 32-63 of this warp's token
             tmem_ld32(tbase, va);
             tmem_ld32(tbase + 32, vb);
-            if constexpr (TPW == 2) {
-                tmem_ld32(tbase + idx::HEADS, vc);
-                tmem_ld32(tbase + idx::HEADS + 32, vd);
-            }
             tmem_ld_wait();
             // the accumulator can be refilled once the registers hold it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_acc_empty[acc]);
-            const long long srow = (long long)b * n_q_rows + i0;
-            const long long tq = q_pos0 + i_start + i0;   // position of token 0 of the group
-            idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, tt0, i0, n_q_rows, tq, m, Nc, scores, srow);
-            if constexpr (TPW == 2)
-                idx_store_score(vc, vd, sq_s + (tt0 + 1) * idx::HEADS, sk, key, tt0 + 1, i0, n_q_rows, tq, m, Nc,
-                                scores, srow);
+            idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr);
         }
     }
 
