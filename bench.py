@@ -206,28 +206,48 @@ def run_decode(args, torch, dist, rank, world):
     torch.cuda.synchronize()
     lib.csa_device_status()
 
-    # ---- timed region: K steps, per-call events ----
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
+    # ---- per-call breakdown: eager steps with CUDA events around each call ----
+    KE = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KE)]
+    for i in range(KE):
+        step(evs[i])
     torch.cuda.synchronize()
-    with ClockSampler(_gpu_id(torch, dev)) as clk:
-        t_start.record(stream)
-        for i in range(K):
-            step(evs[i])
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = t_start.elapsed_time(t_end)
     lib.csa_device_status()
     per = {"indexer": [], "topk": [], "sparse_attn": []}
     for e in evs:
         per["indexer"].append(e[0].elapsed_time(e[1]))
         per["topk"].append(e[1].elapsed_time(e[2]))
         per["sparse_attn"].append(e[2].elapsed_time(e[3]))
+
+    # ---- timed region: K replays of a CUDA graph of one whole step ----
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    lib.csa_device_status()
+    K = args.steps
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(_gpu_id(torch, dev)) as clk:
+        t_start.record(stream)
+        for _ in range(K):
+            graph.replay()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    lib.csa_device_status()
     if dist:
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -306,7 +326,9 @@ def run_decode(args, torch, dist, rank, world):
         cpu = {"value": nq / tt, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{nq} of the 32 decode queries (full 262,144-entry caches), {tt:.1f} s"}
 
-    launches_per_step = 1 + (2 if lib.csa_topk_select_workspace_size(B, 1, Nc, k) else 1) + \
+    # indexer; top-k (sample, collect, select for rows past one CTA's capacity);
+    # attention (+ the slice combine when the key set is split)
+    launches_per_step = 1 + (3 if lib.csa_topk_select_workspace_size(B, 1, Nc, k) else 1) + \
         (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
     res = {
         "metric": METRIC, "value": world * B * K / (ms / 1e3), "unit": "queries/s", "n_gpus": world,
@@ -316,11 +338,13 @@ def run_decode(args, torch, dist, rank, world):
         "config": {"workload": s.name, "batch_per_gpu": B, "ctx_tokens": s.n, "compressed_entries": Nc,
                    "indexer": f"{HI}x{dI} e4m3", "top_k": k, "attention": f"{H}x{d} bf16",
                    "l2": "inputs (5.2 GB per GPU) exceed L2; no flush",
+                   "launch": "one step (indexer, top-k, sparse attention) captured in a CUDA graph and replayed",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "per_call_ms": {kk: round(v, 5) for kk, v in avg.items()},
+        "per_call_note": f"CUDA events around each call of {KE} eager (non-graph) steps",
     }
     return res
 
@@ -429,16 +453,30 @@ def run_config(args, torch, name):
             torch.cuda.synchronize()
             lib.csa_device_status()
             for cname, fn, work, unit, peak in calls:
+                # a CUDA graph of the call, replayed: host-side argument handling
+                # stays out of the measured time
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream()
+                side.wait_stream(stream)
+                with torch.cuda.stream(side):
+                    fn()
+                stream.wait_stream(side)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g):
+                    fn()
+                g.replay()
+                torch.cuda.synchronize()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 for _ in range(args.steps):
-                    fn()
+                    g.replay()
                 b.record(stream)
                 torch.cuda.synchronize()
                 ms = a.elapsed_time(b) / args.steps
                 ach = work / (ms / 1e3) / (1e9 if unit == "GB/s" else 1e12)
                 st[cname] = {"ms": round(ms, 4), "achieved": round(ach, 1), "unit": unit, "peak": peak,
                              "frac": round(ach / peak, 4), "work_per_launch": work}
+                del g
             lib.csa_device_status()
             stages_all[s.name] = st
             del x, calls

@@ -14,8 +14,10 @@
 
 namespace csa {
 
+// At most 64 registers a thread, so at least four CTAs (32 warps) share an SM
+// and keep enough 16-byte loads in flight for HBM when a block is short (m = 4).
 template <typename Tin, int OUT>
-__global__ void __launch_bounds__(256) compress_kernel(int B, int n, int m, int Nc, int d,
+__global__ void __launch_bounds__(256, 4) compress_kernel(int B, int n, int m, int Nc, int d,
                                                        const float* __restrict__ logits,
                                                        const Tin* __restrict__ x, void* out,
                                                        void* out_scale)
@@ -45,7 +47,7 @@ __global__ void __launch_bounds__(256) compress_kernel(int B, int n, int m, int 
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.f;
     const Tin* xp = x + (b * (long long)n + j * (long long)m) * d + 8 * g;
-#pragma unroll 8
+#pragma unroll 4
     for (int i = 0; i < m; ++i) {
         float v[8];
         Vec8<Tin>::load(xp + (long long)i * d, v);

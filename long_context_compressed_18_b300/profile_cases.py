@@ -9,6 +9,7 @@ CUDA-event timings of each case.
     python -m long_context_compressed_18_b300.profile_cases attn [--time]
     python -m long_context_compressed_18_b300.profile_cases indexer [--time]
     python -m long_context_compressed_18_b300.profile_cases topk [--time]
+    python -m long_context_compressed_18_b300.profile_cases compress [--time]
 """
 from __future__ import annotations
 
@@ -95,7 +96,31 @@ def _topk_cases():
              lambda: lib.csa_topk_select(B, 1, (1 << 20) - 1, 4, Nc, k, sc, out, ws, nb))], "GB/s"
 
 
-CASES = {"attn": _attn_cases, "indexer": _indexer_cases, "topk": _topk_cases}
+def _compress_cases():
+    """One stream of the HCA workload (1M tokens, m' = 128, BF16 K -> BF16)
+    and the indexer-K stream of the hybrid stack's CSA layers (131,072 tokens,
+    m = 4, BF16 -> E2M1 with E4M3 block scales)."""
+    g = torch.Generator(device="cpu").manual_seed(14)
+    cases = []
+    for n, m, kind, code in ((1 << 20, 128, "bf16", lib.BF16), (131072, 4, "e2m1", lib.E2M1)):
+        logits = torch.randn(1, n, generator=g).to(DEV)
+        x = torch.randn(1, n, 128, generator=g).to(torch.bfloat16).to(DEV)
+        Nc = n // m
+        if kind == "bf16":
+            out = torch.empty(1, Nc, 128, dtype=torch.bfloat16, device=DEV)
+            sc, obytes = None, Nc * 128 * 2
+        else:
+            out = torch.empty(1, Nc, 64, dtype=torch.uint8, device=DEV)
+            sc, obytes = torch.empty(1, Nc, 4, dtype=torch.uint8, device=DEV), Nc * (64 + 4)
+        work = n * 128 * 2 + n * 4 + obytes
+        cases.append((f"compress_n{n}_m{m}_{kind}", work,
+                      lambda logits=logits, x=x, out=out, sc=sc, n=n, m=m, code=code:
+                      lib.csa_compress(1, n, m, logits, [x], [lib.BF16], [128], [out], [code],
+                                       None if sc is None else [sc])))
+    return cases, "GB/s"
+
+
+CASES = {"attn": _attn_cases, "indexer": _indexer_cases, "topk": _topk_cases, "compress": _compress_cases}
 
 
 def main():
