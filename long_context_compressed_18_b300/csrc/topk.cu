@@ -2,16 +2,17 @@
 // k highest-scoring compressed entries per query).
 //
 // Exact radix select on order-preserving 32-bit keys of the fp32 scores
-// (-0 folded onto +0).  A CTA stages its elements' keys in shared memory,
-// finds the k-th largest key T with three histogram levels (11, 11 and 10
-// bits; see radix_threshold), then writes
-// the selected indices in ascending order with a warp-ballot compaction:
-// every key > T, plus the first (k - #{key > T}) elements equal to T in index
-// order -- i.e. ranking by (score desc, index asc).  No floating-point
-// atomics; the result does not depend on thread scheduling.
+// (-0 folded onto +0): the k-th largest key T is found with three histogram
+// levels (11, 11 and 10 bits; see radix_threshold), and the selection is
+// every key > T plus the first (k - #{key > T}) elements equal to T in index
+// order -- i.e. ranking by (score desc, index asc) -- written in ascending
+// index order.  No floating-point atomics; the result does not depend on
+// thread scheduling.
 //
-// Rows longer than one CTA's capacity (TOPK_MAX_SINGLE) take the three
-// long-row kernels below.
+// Rows up to 16,384 entries take one CTA each with all keys in shared memory;
+// rows up to TOPK_MAX_SINGLE take one fused CTA each (sampled threshold,
+// collection, select); longer rows take three kernels (sample, collect,
+// select) over many CTAs.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -35,6 +36,7 @@ __device__ __forceinline__ uint32_t score_key(float f)
 // the third level.  Rows whose selected bin overflows the list (heavy ties)
 // scan the full key array instead.
 constexpr int CAND_CAP = 2048;
+constexpr int TOPK_SMEM_ROW = 16384;   // rows up to this length stage all their keys in shared memory
 
 struct TopkShared {
     uint32_t hist[2048];
@@ -238,9 +240,10 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
     ordered_compact_by([&](int e) { return keys[e]; }, len, T, take_eq, sh, emit);
 }
 
-// Rows of at most TOPK_MAX_SINGLE entries: one CTA per row, keys staged in
-// shared memory; writes the final indices, -1 padded.
-__global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(
+// Rows of at most TOPK_SMEM_ROW entries: one CTA per row, the row's keys staged
+// in shared memory, one radix select over them and an ordered compaction;
+// writes the final indices, -1 padded.
+__global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc,
     int k, int32_t* __restrict__ out, long long out_b_stride)
 {
@@ -374,29 +377,24 @@ __device__ __forceinline__ void stream_keys(const float* __restrict__ row, int c
     }
 }
 
-__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    LongRowWs w)
+// Collection threshold of a row: the keys of S = min(L, smax) entries in
+// runs of 32 consecutive entries (whole cache lines), evenly spaced, and
+// their key of rank 2 * kk * S / L + 8 (twice the expected rank of the k-th
+// largest key, plus a margin).  keys: shared buffer of smax entries.
+template <int SMAX>
+__device__ uint32_t sample_threshold(const float* __restrict__ row, int L, int kk, uint32_t* keys, TopkShared& sh)
 {
-    __shared__ uint32_t keys[LR_SAMPLES];
-    __shared__ TopkShared sh;
-    const int r = blockIdx.x;
-    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
-    if (threadIdx.x == 0) w.cnt[r] = 0;
-    if (L <= k) return;                           // uniform: the row is copied whole
-    // 128 runs of 32 consecutive entries, evenly spaced (whole cache lines)
-    const int S = L < LR_SAMPLES ? L : LR_SAMPLES;
+    const int S = L < SMAX ? L : SMAX;
     const int runs = S / 32 > 0 ? S / 32 : 1;
-    const float* row = scores + (long long)r * ld;
     clear_hist(sh, 2048);
     __syncthreads();
-    constexpr int U = LR_SAMPLES / TOPK_THREADS;
+    constexpr int U = (SMAX + TOPK_THREADS - 1) / TOPK_THREADS;
     float v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int q = u * TOPK_THREADS + threadIdx.x;
         const int run = q >> 5;
-        const int e = (L < LR_SAMPLES) ? q : (int)((long long)run * (L - 32) / (runs > 1 ? runs - 1 : 1)) + (q & 31);
+        const int e = (L < SMAX) ? q : (int)((long long)run * (L - 32) / (runs > 1 ? runs - 1 : 1)) + (q & 31);
         v[u] = q < S ? __ldg(row + e) : 0.f;
     }
 #pragma unroll
@@ -409,13 +407,26 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
         }
     }
     __syncthreads();
-    // rank of the threshold among the samples: twice the expected rank of the
-    // k-th largest key, plus a margin of 8
-    long long want = 2ll * k * S / L + 8;
+    const long long want = 2ll * kk * S / L + 8;
     const int t_rank = (int)(want < S ? want : S);
     uint32_t T;
     int teq;
     radix_threshold(keys, S, t_rank, sh, T, teq);
+    __syncthreads();
+    return T;
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    LongRowWs w)
+{
+    __shared__ uint32_t keys[LR_SAMPLES];
+    __shared__ TopkShared sh;
+    const int r = blockIdx.x;
+    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
+    if (threadIdx.x == 0) w.cnt[r] = 0;
+    if (L <= k) return;                           // uniform: the row is copied whole
+    const uint32_t T = sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, keys, sh);
     if (threadIdx.x == 0) w.thr[r] = T;
 }
 
@@ -425,33 +436,20 @@ __device__ __forceinline__ float key_value(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    int n_chunks, LongRowWs w)
+// Appends every entry e of [c0, c0 + len) of a row with key >= thr to the
+// shared list (lkey, lidx) of capacity cap through the shared counter *n_loc;
+// *n_loc counts every such entry, even past cap.  key >= thr is tested as the
+// float comparison s >= value(thr), which orders -0 with +0 and never takes a
+// NaN, exactly like the keys; a threshold key of 0 takes every entry.  Each
+// thread builds a take mask over its batch of loads; one warp scan and one
+// shared atomic per batch place the entries.
+__device__ void collect_entries(const float* __restrict__ row, int c0, int len, uint32_t thr, uint32_t* lkey,
+                                int32_t* lidx, uint32_t cap, uint32_t* n_loc)
 {
-    // Entries with key >= thr go to the chunk's shared-memory list, then one
-    // global atomic reserves the chunk's slice of the row's list (whose order
-    // does not matter to the select kernel).  key >= thr is tested as the
-    // float comparison s >= value(thr), which orders -0 with +0 and never
-    // takes a NaN, exactly like the keys; a threshold key of 0 takes all.
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    __shared__ uint32_t n_loc_s, base_s;
-    uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [cap]
-    int32_t* lidx = reinterpret_cast<int32_t*>(lkey + w.cap);
-    const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
-    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
-    if (L <= k) return;
-    const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
-    if (len == 0) return;
-    const uint32_t thr = __ldcg(w.thr + r);
     const bool take_all = thr == 0u;
     const float tf = key_value(thr);
-    if (threadIdx.x == 0) n_loc_s = 0;
-    __syncthreads();
     const int tid = threadIdx.x, lane = tid & 31;
-    const uint32_t cap = (uint32_t)w.cap;
-    const float* src = scores + (long long)r * ld + c0;
-    // reserve warp slots for n entries of this lane; returns the lane's first slot
+    const float* src = row + c0;
     auto reserve = [&](uint32_t n) -> uint32_t {
         uint32_t incl = n;
 #pragma unroll
@@ -461,7 +459,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
         }
         const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
         uint32_t wb = 0;
-        if (lane == 31 && tot) wb = atomicAdd(&n_loc_s, tot);
+        if (lane == 31 && tot) wb = atomicAdd(n_loc, tot);
         wb = __shfl_sync(0xFFFFFFFFu, wb, 31);
         return wb + incl - n;
     };
@@ -525,6 +523,29 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
         for (int u = 0; u < U; ++u)
             if (mask >> u & 1u) put(pos, v[u], base + u * TOPK_THREADS + tid);
     }
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    int n_chunks, LongRowWs w)
+{
+    // the chunk's entries go to a shared-memory list, then one global atomic
+    // reserves the chunk's slice of the row's list (whose order does not
+    // matter to the select kernel)
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ uint32_t n_loc_s, base_s;
+    uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [cap]
+    int32_t* lidx = reinterpret_cast<int32_t*>(lkey + w.cap);
+    const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
+    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
+    if (L <= k) return;
+    const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
+    if (len == 0) return;
+    const uint32_t thr = __ldcg(w.thr + r);
+    if (threadIdx.x == 0) n_loc_s = 0;
+    __syncthreads();
+    const uint32_t cap = (uint32_t)w.cap;
+    collect_entries(scores + (long long)r * ld, c0, len, thr, lkey, lidx, cap, &n_loc_s);
     __syncthreads();
     const uint32_t n_all = n_loc_s;
     if (threadIdx.x == 0) base_s = atomicAdd(w.cnt + r, n_all);   // counts every entry, even past cap
@@ -558,157 +579,137 @@ __device__ uint32_t block_excl_scan(uint32_t v, TopkShared& sh)
     return before;
 }
 
-__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
+// Exact selection among a row's entries (ekey, eidx: n entries in shared
+// memory, every entry of the row whose key is at least some threshold,
+// n >= kk) -- the top kk by (score desc, index asc) -- written to o in
+// ascending index order.  sel and eqm are shared bitmaps of nw = ceil(L / 32)
+// words.
+__device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* sel,
+                               uint32_t* eqm, TopkShared& sh, int32_t* __restrict__ o)
 {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    __shared__ TopkShared sh;
-    const int r = blockIdx.x;
-    const int i = r % n_q_rows;
-    int32_t* o = out + ((long long)(r / n_q_rows) * out_b_stride + i) * k;
-    const int L = visible_len(q_pos0, i, m, Nc);
-    const int kk = min(k, L);
     const int tid = threadIdx.x;
-    for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
-    if (kk == 0) return;
-    if (L <= k) {
-        for (int e = tid; e < L; e += TOPK_THREADS) o[e] = e;
-        return;
+    const int nw = (L + 31) / 32;
+    clear_hist(sh, 2048);
+    for (int x = tid; x < 2 * nw; x += TOPK_THREADS) sel[x] = 0u;   // sel and eqm are adjacent
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        lo = min(lo, ekey[e]);
+        hi = max(hi, ekey[e]);
     }
-    const float* row = scores + (long long)r * ld;
-    const uint32_t got = __ldcg(w.cnt + r);
-    if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
-        // ---- the collected entries (every element with key >= thr) ----
-        const int nw = (L + 31) / 32;
-        uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw);   // [nw] bitmap of selected indices
-        uint32_t* eqm = sel + nw;                                 // [nw] bitmap of keys equal to T
-        uint32_t* ekey = eqm + nw;                                // [cap]
-        int32_t* eidx = reinterpret_cast<int32_t*>(ekey + w.cap);
-        const int n = (int)got;
-        clear_hist(sh, 2048);
-        for (int x = tid; x < 2 * nw; x += TOPK_THREADS) sel[x] = 0u;
-        __syncthreads();
-        const uint32_t thr = __ldcg(w.thr + r);
-        uint32_t span = 0;     // max over entries of key - thr (every entry has key >= thr)
-        for (int base = 0; base < n; base += TOPK_THREADS * 8) {
-            uint32_t kv[8];
-            int32_t iv[8];
+    // Raw keys crowd into a few first-level bins; rank the entries instead by
+    // (key - lo) << s, s putting the top bit of hi - lo at bit 31 -- strictly
+    // increasing in key, so the threshold and the ties (and hence the
+    // selection) are the same, and the first radix level spreads over all
+    // its bins.
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = base + u * TOPK_THREADS + tid;
-                kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : thr;
-                iv[u] = e < n ? __ldcg(w.idx + (size_t)r * w.cap + e) : 0;
+    for (int dd = 16; dd > 0; dd >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
+    }
+    if ((tid & 31) == 0) {
+        sh.scan[tid >> 5] = lo;
+        sh.warp_take[tid >> 5] = hi;
+    }
+    __syncthreads();
+    lo = 0xFFFFFFFFu;
+    hi = 0u;
+    for (int q = 0; q < TOPK_WARPS; ++q) {
+        lo = min(lo, sh.scan[q]);
+        hi = max(hi, sh.warp_take[q]);
+    }
+    const uint32_t span = hi - lo;
+    const int shl = span ? __clz(span) : 0;
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const uint32_t tk = (ekey[e] - lo) << shl;
+        ekey[e] = tk;
+        atomicAdd(&sh.hist[tk >> 21], 1u);
+    }
+    __syncthreads();
+    uint32_t T, n_eq;
+    int teq;
+    radix_threshold(ekey, n, kk, sh, T, teq, &n_eq);
+    __syncthreads();
+    // mark the selection; keys equal to T join it directly unless only some
+    // of them are taken (then the first teq in index order, below)
+    const bool all_eq = n_eq == (uint32_t)teq;
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const uint32_t key = ekey[e];
+        const int j = eidx[e];
+        if (j < 0 || j >= L) continue;
+        if (key > T || (key == T && all_eq)) atomicOr(&sel[j >> 5], 1u << (j & 31));
+        else if (key == T) atomicOr(&eqm[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    const int lane = tid & 31, warp = tid >> 5;
+    if (!all_eq) {
+        // warp-cooperative walk of the tie bitmap: warp w owns words [wa, wb)
+        const int per_w = ((nw + TOPK_WARPS - 1) / TOPK_WARPS + 31) & ~31;
+        const int wa = min(nw, warp * per_w), wb = min(nw, wa + per_w);
+        uint32_t t = 0;
+        for (int x = wa + lane; x < wb; x += 32) t += __popc(eqm[x]);
+#pragma unroll
+        for (int dd = 16; dd > 0; dd >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, dd);
+        if (lane == 0) sh.scan[warp] = t;
+        __syncthreads();
+        uint32_t rank = 0;
+        for (int q = 0; q < warp; ++q) rank += sh.scan[q];
+        for (int x0 = wa; x0 < wb; x0 += 32) {
+            const int x = x0 + lane;
+            uint32_t bits = x < wb ? eqm[x] : 0u;
+            const uint32_t nb = __popc(bits);
+            uint32_t incl = nb;
+#pragma unroll
+            for (int dd = 1; dd < 32; dd <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, dd);
+                if (lane >= dd) incl += v;
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = base + u * TOPK_THREADS + tid;
-                if (e < n) {
-                    ekey[e] = kv[u];
-                    eidx[e] = iv[u];
-                    span = max(span, kv[u] - thr);
-                }
-            }
-        }
-        // The entries crowd into one or two first-level bins of the raw keys;
-        // rank them instead by (key - thr) << s, s putting the top bit of the
-        // span at bit 31 -- strictly increasing in key, so the threshold and
-        // the ties (and hence the selection) are the same, and the first
-        // radix level spreads over all its bins.
-#pragma unroll
-        for (int dd = 16; dd > 0; dd >>= 1) span = max(span, __shfl_xor_sync(0xFFFFFFFFu, span, dd));
-        if ((tid & 31) == 0) sh.scan[tid >> 5] = span;
-        __syncthreads();
-        span = 0;
-        for (int q = 0; q < TOPK_WARPS; ++q) span = max(span, sh.scan[q]);
-        const int shl = span ? __clz(span) : 0;
-        for (int e = tid; e < n; e += TOPK_THREADS) {
-            const uint32_t tk = (ekey[e] - thr) << shl;
-            ekey[e] = tk;
-            atomicAdd(&sh.hist[tk >> 21], 1u);
-        }
-        __syncthreads();
-        uint32_t T, n_eq;
-        int teq;
-        radix_threshold(ekey, n, kk, sh, T, teq, &n_eq);
-        __syncthreads();
-        // mark the selection; keys equal to T join it directly unless only some
-        // of them are taken (then the first teq in index order, below)
-        const bool all_eq = n_eq == (uint32_t)teq;
-        for (int e = tid; e < n; e += TOPK_THREADS) {
-            const uint32_t key = ekey[e];
-            const int j = eidx[e];
-            if (j < 0 || j >= L) continue;
-            if (key > T || (key == T && all_eq)) atomicOr(&sel[j >> 5], 1u << (j & 31));
-            else if (key == T) atomicOr(&eqm[j >> 5], 1u << (j & 31));
-        }
-        __syncthreads();
-        const int lane = tid & 31, warp = tid >> 5;
-        if (!all_eq) {
-            // warp-cooperative walk of the tie bitmap: warp w owns words [wa, wb)
-            const int per_w = ((nw + TOPK_WARPS - 1) / TOPK_WARPS + 31) & ~31;
-            const int wa = min(nw, warp * per_w), wb = min(nw, wa + per_w);
-            uint32_t t = 0;
-            for (int x = wa + lane; x < wb; x += 32) t += __popc(eqm[x]);
-#pragma unroll
-            for (int dd = 16; dd > 0; dd >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, dd);
-            if (lane == 0) sh.scan[warp] = t;
-            __syncthreads();
-            uint32_t rank = 0;
-            for (int q = 0; q < warp; ++q) rank += sh.scan[q];
-            for (int x0 = wa; x0 < wb; x0 += 32) {
-                const int x = x0 + lane;
-                uint32_t bits = x < wb ? eqm[x] : 0u;
-                const uint32_t nb = __popc(bits);
-                uint32_t incl = nb;
-#pragma unroll
-                for (int dd = 1; dd < 32; dd <<= 1) {
-                    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, dd);
-                    if (lane >= dd) incl += v;
-                }
-                const uint32_t r0 = rank + incl - nb;
-                if (bits) {
-                    if (r0 + nb <= (uint32_t)teq) {
-                        sel[x] |= bits;
-                    } else if (r0 < (uint32_t)teq) {
-                        for (uint32_t q = r0; q < (uint32_t)teq; ++q) {
-                            const uint32_t low = bits & (0u - bits);
-                            sel[x] |= low;
-                            bits ^= low;
-                        }
+            const uint32_t r0 = rank + incl - nb;
+            if (bits) {
+                if (r0 + nb <= (uint32_t)teq) {
+                    sel[x] |= bits;
+                } else if (r0 < (uint32_t)teq) {
+                    for (uint32_t q = r0; q < (uint32_t)teq; ++q) {
+                        const uint32_t low = bits & (0u - bits);
+                        sel[x] |= low;
+                        bits ^= low;
                     }
                 }
-                rank += __shfl_sync(0xFFFFFFFFu, incl, 31);
             }
-            __syncthreads();
-        }
-        // output slot of index j: (selected indices in words before j's) +
-        // (selected bits below j in its word); the per-word prefix goes into
-        // the tie bitmap's storage
-        uint32_t* wpre = eqm;
-        const int per_t = (nw + TOPK_THREADS - 1) / TOPK_THREADS;
-        const int t0 = min(nw, tid * per_t), t1 = min(nw, t0 + per_t);
-        uint32_t cntw = 0;
-        for (int x = t0; x < t1; ++x) cntw += __popc(sel[x]);
-        uint32_t run = block_excl_scan(cntw, sh);
-        for (int x = t0; x < t1; ++x) {
-            const uint32_t c = __popc(sel[x]);
-            wpre[x] = run;
-            run += c;
+            rank += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
         __syncthreads();
-        for (int e = tid; e < n; e += TOPK_THREADS) {
-            const int j = eidx[e];
-            if (j < 0 || j >= L) continue;
-            const uint32_t word = sel[j >> 5], bit = 1u << (j & 31);
-            if (word & bit) {
-                const uint32_t pos = wpre[j >> 5] + __popc(word & (bit - 1u));
-                if (pos < (uint32_t)kk) o[pos] = j;
-            }
-        }
-        return;
     }
-    // ---- heavy ties or a misjudged sample: stream the row from global memory ----
+    // output slot of index j: (selected indices in words before j's) +
+    // (selected bits below j in its word); the per-word prefix goes into
+    // the tie bitmap's storage
+    uint32_t* wpre = eqm;
+    const int per_t = (nw + TOPK_THREADS - 1) / TOPK_THREADS;
+    const int t0 = min(nw, tid * per_t), t1 = min(nw, t0 + per_t);
+    uint32_t cntw = 0;
+    for (int x = t0; x < t1; ++x) cntw += __popc(sel[x]);
+    uint32_t run = block_excl_scan(cntw, sh);
+    for (int x = t0; x < t1; ++x) {
+        const uint32_t c = __popc(sel[x]);
+        wpre[x] = run;
+        run += c;
+    }
+    __syncthreads();
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const int j = eidx[e];
+        if (j < 0 || j >= L) continue;
+        const uint32_t word = sel[j >> 5], bit = 1u << (j & 31);
+        if (word & bit) {
+            const uint32_t pos = wpre[j >> 5] + __popc(word & (bit - 1u));
+            if (pos < (uint32_t)kk) o[pos] = j;
+        }
+    }
+}
+
+// Exact selection of a row's top kk streamed from global memory: the three
+// radix levels, then the ordered compaction.
+__device__ void select_streaming(const float* __restrict__ row, int L, int kk, TopkShared& sh,
+                                 int32_t* __restrict__ o)
+{
     clear_hist(sh, 2048);
     __syncthreads();
     stream_keys(row, 0, L, [&](bool in, int, uint32_t key) {
@@ -738,6 +739,115 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const int teq = (int)(rem - sh.above);
     ordered_compact_by([&](int e) { return score_key(__ldg(row + e)); }, L, T, teq, sh,
                        [&](int pos, int e) { if (pos < kk) o[pos] = e; });
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ TopkShared sh;
+    const int r = blockIdx.x;
+    const int i = r % n_q_rows;
+    int32_t* o = out + ((long long)(r / n_q_rows) * out_b_stride + i) * k;
+    const int L = visible_len(q_pos0, i, m, Nc);
+    const int kk = min(k, L);
+    const int tid = threadIdx.x;
+    for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
+    if (kk == 0) return;
+    if (L <= k) {
+        for (int e = tid; e < L; e += TOPK_THREADS) o[e] = e;
+        return;
+    }
+    const float* row = scores + (long long)r * ld;
+    const uint32_t got = __ldcg(w.cnt + r);
+    if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
+        const int nw = (L + 31) / 32;
+        uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw);   // [nw] bitmap of selected indices
+        uint32_t* eqm = sel + nw;                                 // [nw] bitmap of keys equal to T
+        uint32_t* ekey = eqm + nw;                                // [cap]
+        int32_t* eidx = reinterpret_cast<int32_t*>(ekey + w.cap);
+        const int n = (int)got;
+        for (int base = 0; base < n; base += TOPK_THREADS * 8) {
+            uint32_t kv[8];
+            int32_t iv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = base + u * TOPK_THREADS + tid;
+                kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : 0u;
+                iv[u] = e < n ? __ldcg(w.idx + (size_t)r * w.cap + e) : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = base + u * TOPK_THREADS + tid;
+                if (e < n) {
+                    ekey[e] = kv[u];
+                    eidx[e] = iv[u];
+                }
+            }
+        }
+        __syncthreads();
+        select_entries(ekey, eidx, n, kk, L, sel, eqm, sh, o);
+        return;
+    }
+    select_streaming(row, L, kk, sh, o);
+}
+
+// ---------------------------------------------------------------------------
+// Rows of at most TOPK_MAX_SINGLE entries: one CTA per row runs the same
+// steps as the long-row kernels, fused -- a sampled threshold (or the whole
+// row when it fits the entry list), one collection pass into shared memory,
+// the exact select over the entries -- with the streamed route for rows whose
+// sample misjudges them.  About 57 KB of shared memory at k = 1024 and at most
+// 64 registers a thread, so two rows run per SM.
+// ---------------------------------------------------------------------------
+constexpr int ROW_SAMPLES = 2048;
+
+// Entry-list capacity of the fused kernel: enough for about twice k
+// collected entries (rows that fit take everything, no sampling).
+static int row_cap(int N_c, int k)
+{
+    (void)N_c;
+    return 2 * k + 2048 > 4096 ? 2 * k + 2048 : 4096;
+}
+
+static size_t row_smem_bytes(int N_c, int k) { return (size_t)row_cap(N_c, k) * 8 + (size_t)2 * ((N_c + 31) / 32) * 4; }
+
+__global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
+    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k, int cap,
+    int32_t* __restrict__ out, long long out_b_stride)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ TopkShared sh;
+    __shared__ uint32_t n_cnt;
+    uint32_t* ekey = reinterpret_cast<uint32_t*>(smem_raw);   // [cap]; holds the samples first
+    int32_t* eidx = reinterpret_cast<int32_t*>(ekey + cap);   // [cap]
+    uint32_t* bitmaps = reinterpret_cast<uint32_t*>(eidx + cap);
+    const int r = (int)blockIdx.x;
+    const int i = r % n_q_rows;   // query index within the chunk of rows
+    int32_t* o = out + ((long long)(r / n_q_rows) * out_b_stride + i) * k;
+    const int L = visible_len(q_pos0, i, m, Nc);
+    const int kk = min(k, L);
+    const int tid = threadIdx.x;
+    for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
+    if (kk == 0) return;
+    if (L <= k) {
+        for (int e = tid; e < L; e += TOPK_THREADS) o[e] = e;
+        return;
+    }
+    const float* row = scores + (long long)r * ld;
+    const uint32_t thr = L > cap ? sample_threshold<ROW_SAMPLES>(row, L, kk, ekey, sh) : 0u;   // 0: take all
+    if (tid == 0) n_cnt = 0;
+    __syncthreads();
+    collect_entries(row, 0, L, thr, ekey, eidx, (uint32_t)cap, &n_cnt);
+    __syncthreads();
+    const uint32_t n = n_cnt;
+    if (n >= (uint32_t)kk && n <= (uint32_t)cap) {
+        const int nw = (L + 31) / 32;
+        select_entries(ekey, eidx, (int)n, kk, L, bitmaps, bitmaps + nw, sh, o);
+        return;
+    }
+    select_streaming(row, L, kk, sh, o);
 }
 
 // Chunking plan shared by the launcher and the workspace query.
@@ -771,10 +881,17 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
     const int rows = B * n_q_rows;
     if (rows == 0) return cudaSuccess;
     TopkPlan p = topk_plan(N_c, k);
+    if (p.n_chunks == 1 && N_c <= TOPK_SMEM_ROW) {
+        const size_t smem = (size_t)(N_c > 0 ? N_c : 1) * sizeof(uint32_t);
+        cudaFuncSetAttribute(topk_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        topk_smem_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
+        return cudaGetLastError();
+    }
     if (p.n_chunks == 1) {
-        size_t smem = (size_t)p.chunk * sizeof(uint32_t);
+        const size_t smem = row_smem_bytes(N_c, k);
         cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        topk_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
+        topk_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, row_cap(N_c, k), out,
+                                                     out_b_stride);
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
