@@ -352,10 +352,21 @@ csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_stream
         }
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int kinds[4];
+    bool bf16_in[4];
     for (int s = 0; s < n_streams; ++s) {
-        const int kind = out_dtype[s] == CSA_F32 ? 0 : out_dtype[s] == CSA_BF16 ? 1 : out_dtype[s] == CSA_E4M3 ? 2 : 3;
-        cudaError_t e = launch_compress(B, n, m, dim[s], logits, x[s], x_dtype[s] == CSA_BF16, out[s], kind,
-                                        out_scale ? out_scale[s] : nullptr, st);
+        kinds[s] = out_dtype[s] == CSA_F32 ? 0 : out_dtype[s] == CSA_BF16 ? 1 : out_dtype[s] == CSA_E4M3 ? 2 : 3;
+        bf16_in[s] = x_dtype[s] == CSA_BF16;
+    }
+    if (compress_tiles_supported(n, m, n_streams, dim, bf16_in)) {
+        cudaError_t e = launch_compress_tiles(B, n, m, n_streams, logits, x, bf16_in, dim, out, kinds, out_scale,
+                                              num_sms(), st);
+        if (e != cudaSuccess) return cuda_status(e, "compress launch");
+        return CSA_OK;
+    }
+    for (int s = 0; s < n_streams; ++s) {
+        cudaError_t e = launch_compress(B, n, m, dim[s], logits, x[s], bf16_in[s], out[s], kinds[s],
+                                        out_scale ? out_scale[s] : nullptr, num_sms(), st);
         if (e != cudaSuccess) return cuda_status(e, "compress launch");
     }
     return CSA_OK;

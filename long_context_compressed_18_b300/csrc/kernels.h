@@ -20,7 +20,14 @@ csa_status_t report(csa_status_t st, const char* msg);
 // ---- compression ----
 // out_kind: 0 f32, 1 bf16, 2 e4m3 (+ fp32 row scale), 3 e2m1 (+ e4m3 block scales)
 cudaError_t launch_compress(int B, int n, int m, int d, const float* logits, const void* x, bool x_bf16,
-                            void* out, int out_kind, void* out_scale, cudaStream_t s);
+                            void* out, int out_kind, void* out_scale, int num_sms, cudaStream_t s);
+// All streams in one launch, for short blocks (4 <= m <= 32, m and n multiples
+// of 4, one tile entry within the stage budget); out_kind 0 f32, 1 bf16,
+// 2 e4m3, 3 e2m1.
+bool compress_tiles_supported(int n, int m, int n_streams, const int* dim, const bool* x_bf16);
+cudaError_t launch_compress_tiles(int B, int n, int m, int n_streams, const float* logits, const void* const* x,
+                                  const bool* x_bf16, const int* dim, void* const* out, const int* out_kind,
+                                  void* const* out_scale, int num_sms, cudaStream_t s);
 
 // ---- top-k ----
 constexpr int TOPK_MAX_SINGLE = 32768;   // entries one CTA selects from (keys in smem)

@@ -4,7 +4,8 @@ Each case calls the C ABI on seeded N(0,1) inputs that are larger than L2
 where the kernel streams (so DRAM counters mean something) but small enough
 for an ``ncu --set full`` capture to end in a minute or two.  Every case runs
 twice, so a capture can skip the first (cold) round; ``--time`` also prints
-CUDA-event timings of each case.
+CUDA-event timings of each case: 20 replays of a CUDA graph of the call, and
+20 eager calls.
 
     python -m long_context_compressed_18_b300.profile_cases attn [--time]
     python -m long_context_compressed_18_b300.profile_cases indexer [--time]
@@ -135,6 +136,7 @@ def main():
     torch.cuda.synchronize()
     lib.csa_device_status()
     if a.time:
+        scale = 1e12 if unit == "TFLOP/s" else 1e9
         for name, work, fn in cases:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -142,9 +144,27 @@ def main():
                 fn()
             e1.record()
             torch.cuda.synchronize()
+            eager = e0.elapsed_time(e1) / 20
+            # the same call captured once in a CUDA graph and replayed: device
+            # time without the host's launch overhead
+            graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fn()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph):
+                fn()
+            for _ in range(3):
+                graph.replay()
+            e0.record()
+            for _ in range(20):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / 20
-            rate = work / (ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
-            print(f"{name}: {ms:.4f} ms  {rate:.1f} {unit}")
+            print(f"{name}: {ms:.4f} ms  {work / (ms / 1e3) / scale:.1f} {unit} (graph replay); "
+                  f"eager {eager:.4f} ms")
         lib.csa_device_status()
 
 

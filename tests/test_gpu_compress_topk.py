@@ -102,6 +102,110 @@ def test_quantised_compression_within_format_error():
     assert (host(packed).numpy() != wp).mean() < 2e-3
 
 
+def _check_e4m3(codes, scale, ref32, what):
+    """E4M3 rows against the oracle's quantiser on the fp32-rounded oracle
+    compression: scales to 1e-6, codes at most one E4M3 step apart and rarely."""
+    wc, ws = oracle.quant_e4m3_rows(ref32)
+    c, s = host(codes).numpy(), host(scale).numpy()
+    assert_close(s, ws, atol=0, rtol=1e-6, what=f"{what} e4m3 scales")
+    dec = oracle.e4m3_decode(c).astype(np.float64) * s[..., None]
+    ref = oracle.e4m3_decode(wc).astype(np.float64) * ws[..., None]
+    step = np.abs(ref) * 2.0 ** -3 + s[..., None] * 2.0 ** -9 + 1e-12
+    assert np.all(np.abs(dec - ref) <= step * 1.0001), what
+    assert (c != wc).mean() < 1e-3, what
+
+
+def _check_e2m1(packed, sc, ref32, what):
+    wp, wsc = oracle.quant_e2m1_blocks(ref32)
+    assert (host(sc).numpy() != wsc).mean() < 1e-3, what
+    assert (host(packed).numpy() != wp).mean() < 2e-3, what
+
+
+def _alloc_out(B, Nc, d, kind):
+    if kind == lib.E4M3:
+        return (torch.empty(B, Nc, d, dtype=torch.uint8, device=DEV),
+                torch.empty(B, Nc, dtype=torch.float32, device=DEV))
+    if kind == lib.E2M1:
+        return (torch.empty(B, Nc, d // 2, dtype=torch.uint8, device=DEV),
+                torch.empty(B, Nc, d // 32, dtype=torch.uint8, device=DEV))
+    dt = torch.float32 if kind == lib.F32 else torch.bfloat16
+    return torch.empty(B, Nc, d, dtype=dt, device=DEV), None
+
+
+def _check_stream(got, sc, want64, kind, what):
+    if kind == lib.F32:
+        assert_close(host(got).numpy(), want64, atol=2e-6, rtol=2e-6, what=what)
+    elif kind == lib.BF16:
+        assert_close(host(got).float().numpy(), want64, atol=1e-6, rtol=2.0 ** -8 + 1e-5, what=what)
+    elif kind == lib.E4M3:
+        _check_e4m3(got, sc, want64.astype(np.float32), what)
+    else:
+        _check_e2m1(got, sc, want64.astype(np.float32), what)
+
+
+# Short blocks with m and n multiples of 4 take the tiled all-streams kernel:
+# one call mixing input dtypes, widths and every output kind, with a batch of
+# two and an entry count that leaves a ragged last tile.
+@pytest.mark.parametrize("m", [4, 8, 16, 32])
+def test_compress_tiles_mixed_streams(m):
+    g = torch.Generator().manual_seed(300 + m)
+    B, Nc = 2, 1237
+    n = Nc * m + (4 if m > 4 else 0)         # a ragged partial block at the end
+    if m < 32:
+        spec = [(torch.float32, 64, lib.F32), (torch.bfloat16, 128, lib.BF16),
+                (torch.bfloat16, 128, lib.E4M3), (torch.float32, 32, lib.E2M1)]
+    else:
+        spec = [(torch.bfloat16, 128, lib.BF16), (torch.float32, 32, lib.E2M1)]
+    logits = torch.randn(B, n, generator=g) * 2
+    xs = [torch.randn(B, n, d, generator=g).to(dt) for dt, d, _ in spec]
+    outs = [_alloc_out(B, Nc, d, k) for _, d, k in spec]
+    lib.csa_compress(B, n, m, logits.to(DEV), [x.to(DEV) for x in xs],
+                     [lib.F32 if dt == torch.float32 else lib.BF16 for dt, _, _ in spec],
+                     [d for _, d, _ in spec], [o for o, _ in outs], [k for _, _, k in spec],
+                     [sc for _, sc in outs])
+    sync_status()
+    for (dt, d, kind), x, (o, sc) in zip(spec, xs, outs):
+        _check_stream(o, sc, oracle.compress(logits, x, m), kind, f"m={m} d={d} kind={kind}")
+
+
+def test_compress_tiles_extremes():
+    """Closed forms through the tiled kernel: equal logits give the block
+    mean; one dominant logit selects its token; a tiny batch of one entry."""
+    g = torch.Generator().manual_seed(310)
+    B, m, Nc, d = 1, 4, 513, 128
+    n = Nc * m
+    x = torch.randn(B, n, d, generator=g).to(torch.bfloat16)
+    out, _ = _compress(x.to(DEV), torch.zeros(B, n).to(DEV), m, lib.F32)
+    mean = x.float().view(B, Nc, m, d).double().mean(2).numpy()
+    assert_close(host(out).numpy(), mean, atol=1e-6, rtol=1e-6, what="equal logits -> block mean")
+    logits = torch.zeros(B, n)
+    pick = torch.randint(0, m, (Nc,), generator=g)
+    logits[0, torch.arange(Nc) * m + pick] = 1e4
+    out, _ = _compress(x.to(DEV), logits.to(DEV), m, lib.F32)
+    sel = x.float().view(B, Nc, m, d)[0, torch.arange(Nc), pick].numpy()[None]
+    assert np.array_equal(host(out).numpy(), sel)
+    x1 = torch.randn(1, 4, 128, generator=g)
+    l1 = torch.randn(1, 4, generator=g)
+    out, _ = _compress(x1.to(DEV), l1.to(DEV), 4, lib.F32)
+    assert_close(host(out).numpy(), oracle.compress(l1, x1, 4), atol=2e-6, rtol=2e-6, what="one entry")
+
+
+def test_compress_tiles_stack_size():
+    """The hybrid stack's CSA compression at full size: 131,072 tokens, m = 4,
+    K and V to BF16 and the indexer key to E2M1, every entry checked."""
+    g = torch.Generator().manual_seed(320)
+    B, n, m, d = 1, 131072, 4, 128
+    logits = torch.randn(B, n, generator=g)
+    xs = [torch.randn(B, n, d, generator=g).to(torch.bfloat16) for _ in range(3)]
+    kinds = [lib.BF16, lib.BF16, lib.E2M1]
+    outs = [_alloc_out(B, n // m, d, k) for k in kinds]
+    lib.csa_compress(B, n, m, logits.to(DEV), [x.to(DEV) for x in xs], [lib.BF16] * 3, [d] * 3,
+                     [o for o, _ in outs], kinds, [sc for _, sc in outs])
+    sync_status()
+    for x, kind, (o, sc) in zip(xs, kinds, outs):
+        _check_stream(o, sc, oracle.compress(logits, x, m), kind, f"stack kind={kind}")
+
+
 # ---- top-k on identical scores: bit-exact --------------------------------
 
 def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed, order=None):
