@@ -276,13 +276,14 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
 
 // ---------------------------------------------------------------------------
 // Long rows (more than one CTA's capacity): three kernels.
-//   sample   one CTA per row: keys of 4096 evenly spaced entries; their key
-//            of rank ~2k * 4096 / L (plus a margin) becomes the row's
-//            collection threshold thr, expected to sit well below the k-th
-//            largest key;
+//   sample   one CTA per row: keys of 4096 evenly spaced entries; a key at
+//            or below their key of rank ~2k * 4096 / L (plus a margin)
+//            becomes the row's collection threshold thr, expected to sit
+//            well below the k-th largest key;
 //   collect  one CTA per 16384-entry chunk: every entry with key >= thr is
-//            appended to the chunk's shared-memory list, whose slice of the
-//            row's entry list is then reserved with one global atomic;
+//            appended to the chunk's shared-memory list (4096 entries),
+//            whose slice of the row's entry list is then reserved with one
+//            global atomic;
 //   select   one CTA per row: if the row collected at least k entries (so
 //            the k-th largest key T is >= thr and every entry with key >= T
 //            was collected) and no more than the list holds, the exact
@@ -296,6 +297,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
 // ---------------------------------------------------------------------------
 constexpr int LR_CHUNK = 16384;
 constexpr int LR_SAMPLES = 4096;
+constexpr int LR_LOCAL_CAP = 4096;   // a chunk's shared-memory list (32 KB: four CTAs an SM)
 
 static int lr_cap(int k) { return k * 4 > 8192 ? k * 4 : 8192; }
 
@@ -378,40 +380,80 @@ __device__ __forceinline__ void stream_keys(const float* __restrict__ row, int c
 }
 
 // Collection threshold of a row: the keys of S = min(L, smax) entries in
-// runs of 32 consecutive entries (whole cache lines), evenly spaced, and
-// their key of rank 2 * kk * S / L + 8 (twice the expected rank of the k-th
-// largest key, plus a margin).  keys: shared buffer of smax entries.
+// runs of 32 consecutive entries (whole cache lines), evenly spaced, ranked at
+// t = 2 * kk * S / L + 8 (twice the expected rank of the k-th largest key,
+// plus a margin).  The threshold only has to lie at or below the sample key
+// of rank t: the samples' keys are spread as (key - lo) << s, s putting the
+// top bit of hi - lo at bit 31, two histogram levels (bits 31..21, then 20..10
+// within the selected bin) locate rank t, and the lowest key whose spread key
+// falls in that second-level bin is returned.  keys: shared buffer of smax
+// entries.
 template <int SMAX>
 __device__ uint32_t sample_threshold(const float* __restrict__ row, int L, int kk, uint32_t* keys, TopkShared& sh)
 {
     const int S = L < SMAX ? L : SMAX;
     const int runs = S / 32 > 0 ? S / 32 : 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     clear_hist(sh, 2048);
-    __syncthreads();
     constexpr int U = (SMAX + TOPK_THREADS - 1) / TOPK_THREADS;
+    // run starts at run * (L - 32) / (runs - 1), in 24.8 fixed point: at most
+    // (L - 32), so every sampled run lies inside the row
+    const uint64_t step = ((uint64_t)(L > 32 ? L - 32 : 0) << 8) / (uint64_t)(runs > 1 ? runs - 1 : 1);
     float v[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int q = u * TOPK_THREADS + threadIdx.x;
+        const int q = u * TOPK_THREADS + tid;
         const int run = q >> 5;
-        const int e = (L < SMAX) ? q : (int)((long long)run * (L - 32) / (runs > 1 ? runs - 1 : 1)) + (q & 31);
+        const int e = (L < SMAX) ? q : (int)(((uint64_t)run * step) >> 8) + (q & 31);
         v[u] = q < S ? __ldg(row + e) : 0.f;
     }
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int q = u * TOPK_THREADS + threadIdx.x;
+        const int q = u * TOPK_THREADS + tid;
         if (q < S) {
             const uint32_t key = score_key(v[u]);
             keys[q] = key;
-            atomicAdd(&sh.hist[key >> 21], 1u);
+            lo = min(lo, key);
+            hi = max(hi, key);
         }
     }
+#pragma unroll
+    for (int dd = 16; dd > 0; dd >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
+    }
+    if (lane == 0) {
+        sh.scan[warp] = lo;
+        sh.warp_take[warp] = hi;
+    }
+    __syncthreads();
+    lo = 0xFFFFFFFFu;
+    hi = 0u;
+    for (int q = 0; q < TOPK_WARPS; ++q) {
+        lo = min(lo, sh.scan[q]);
+        hi = max(hi, sh.warp_take[q]);
+    }
+    const uint32_t span = hi - lo;
+    const int shl = span ? __clz(span) : 0;
+    for (int q = tid; q < S; q += TOPK_THREADS) atomicAdd(&sh.hist[((keys[q] - lo) << shl) >> 21], 1u);
     __syncthreads();
     const long long want = 2ll * kk * S / L + 8;
     const int t_rank = (int)(want < S ? want : S);
-    uint32_t T;
-    int teq;
-    radix_threshold(keys, S, t_rank, sh, T, teq);
+    find_bin<2048>(sh, (uint32_t)t_rank);
+    const uint32_t b1 = sh.bin, rem = (uint32_t)t_rank - sh.above;
+    // second level: bits 20..10 of the spread keys in that bin
+    clear_hist(sh, 2048);
+    __syncthreads();
+    for (int q = tid; q < S; q += TOPK_THREADS) {
+        const uint32_t sk = (keys[q] - lo) << shl;
+        if ((sk >> 21) == b1) atomicAdd(&sh.hist[(sk >> 10) & 0x7FFu], 1u);
+    }
+    __syncthreads();
+    find_bin<2048>(sh, rem);
+    // the lowest key whose spread key reaches the bin's: lo + ceil(sk / 2^shl)
+    const uint64_t sk = ((uint64_t)b1 << 21) | ((uint64_t)sh.bin << 10);
+    const uint32_t T = lo + (uint32_t)((sk + ((1ull << shl) - 1ull)) >> shl);
     __syncthreads();
     return T;
 }
@@ -534,8 +576,8 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     // matter to the select kernel)
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t n_loc_s, base_s;
-    uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [cap]
-    int32_t* lidx = reinterpret_cast<int32_t*>(lkey + w.cap);
+    uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [LR_LOCAL_CAP]
+    int32_t* lidx = reinterpret_cast<int32_t*>(lkey + LR_LOCAL_CAP);
     const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
     const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
     if (L <= k) return;
@@ -545,12 +587,16 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     if (threadIdx.x == 0) n_loc_s = 0;
     __syncthreads();
     const uint32_t cap = (uint32_t)w.cap;
-    collect_entries(scores + (long long)r * ld, c0, len, thr, lkey, lidx, cap, &n_loc_s);
+    collect_entries(scores + (long long)r * ld, c0, len, thr, lkey, lidx, LR_LOCAL_CAP, &n_loc_s);
     __syncthreads();
     const uint32_t n_all = n_loc_s;
-    if (threadIdx.x == 0) base_s = atomicAdd(w.cnt + r, n_all);   // counts every entry, even past cap
+    // counts every entry, even past the row's capacity; a chunk that
+    // overflowed its own list pushes the count past it too, so the row is
+    // selected by the streamed route
+    if (threadIdx.x == 0)
+        base_s = atomicAdd(w.cnt + r, n_all + (n_all > (uint32_t)LR_LOCAL_CAP ? cap + 1u : 0u));
     __syncthreads();
-    const uint32_t base = base_s, n_loc = min(n_all, cap);
+    const uint32_t base = base_s, n_loc = min(n_all, (uint32_t)LR_LOCAL_CAP);
     uint32_t* ek = w.key + (size_t)r * cap;
     int32_t* ei = w.idx + (size_t)r * cap;
     for (uint32_t q = threadIdx.x; q < n_loc; q += TOPK_THREADS) {
@@ -561,36 +607,24 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     }
 }
 
-// Block-wide exclusive prefix sum of one value per thread.
-__device__ uint32_t block_excl_scan(uint32_t v, TopkShared& sh)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    __syncthreads();
-    if (lane == 31) sh.scan[warp] = incl;
-    __syncthreads();
-    uint32_t before = incl - v;
-    for (int w = 0; w < warp; ++w) before += sh.scan[w];
-    return before;
-}
+// Words of one index bitmap of a row of L entries, rounded up to whole
+// 16-byte groups.
+__host__ __device__ constexpr int bitmap_words(int L) { return (((L + 31) / 32) + 3) & ~3; }
 
 // Exact selection among a row's entries (ekey, eidx: n entries in shared
 // memory, every entry of the row whose key is at least some threshold,
 // n >= kk) -- the top kk by (score desc, index asc) -- written to o in
-// ascending index order.  sel and eqm are shared bitmaps of nw = ceil(L / 32)
-// words.
-__device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* sel,
-                               uint32_t* eqm, TopkShared& sh, int32_t* __restrict__ o)
+// ascending index order.  bitmaps: shared memory for two bitmaps of
+// bitmap_words(L) words each (16-byte aligned).
+__device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* bitmaps,
+                               TopkShared& sh, int32_t* __restrict__ o)
 {
     const int tid = threadIdx.x;
-    const int nw = (L + 31) / 32;
+    const int nw = (L + 31) / 32, nw4 = bitmap_words(L);
+    uint32_t* sel = bitmaps;
+    uint32_t* eqm = bitmaps + nw4;
     clear_hist(sh, 2048);
-    for (int x = tid; x < 2 * nw; x += TOPK_THREADS) sel[x] = 0u;   // sel and eqm are adjacent
+    for (int x = tid; x < 2 * nw4; x += TOPK_THREADS) bitmaps[x] = 0u;
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
     for (int e = tid; e < n; e += TOPK_THREADS) {
         lo = min(lo, ekey[e]);
@@ -681,17 +715,41 @@ __device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int k
     }
     // output slot of index j: (selected indices in words before j's) +
     // (selected bits below j in its word); the per-word prefix goes into
-    // the tie bitmap's storage
+    // the tie bitmap's storage.  Warp w owns words [wa, wb): its lanes read
+    // consecutive words (no bank conflicts) and a warp scan carries the count.
     uint32_t* wpre = eqm;
-    const int per_t = (nw + TOPK_THREADS - 1) / TOPK_THREADS;
-    const int t0 = min(nw, tid * per_t), t1 = min(nw, t0 + per_t);
-    uint32_t cntw = 0;
-    for (int x = t0; x < t1; ++x) cntw += __popc(sel[x]);
-    uint32_t run = block_excl_scan(cntw, sh);
-    for (int x = t0; x < t1; ++x) {
-        const uint32_t c = __popc(sel[x]);
-        wpre[x] = run;
-        run += c;
+    {
+        const int nq = nw4 / 4;   // 16-byte groups of words; a lane takes one group a step
+        const int per_w = ((nq + TOPK_WARPS - 1) / TOPK_WARPS + 31) & ~31;
+        const int qa = min(nq, warp * per_w), qb = min(nq, qa + per_w);
+        const uint4* sel4 = reinterpret_cast<const uint4*>(sel);
+        uint4* wpre4 = reinterpret_cast<uint4*>(wpre);
+        uint32_t t = 0;
+        for (int q = qa + lane; q < qb; q += 32) {
+            const uint4 w4 = sel4[q];
+            t += __popc(w4.x) + __popc(w4.y) + __popc(w4.z) + __popc(w4.w);
+        }
+#pragma unroll
+        for (int dd = 16; dd > 0; dd >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, dd);
+        if (lane == 0) sh.scan[warp] = t;
+        __syncthreads();
+        uint32_t run = 0;
+        for (int q = 0; q < warp; ++q) run += sh.scan[q];
+        for (int q0 = qa; q0 < qb; q0 += 32) {
+            const int q = q0 + lane;
+            const uint4 w4 = q < qb ? sel4[q] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t c0 = __popc(w4.x), c1 = __popc(w4.y), c2 = __popc(w4.z), c3 = __popc(w4.w);
+            const uint32_t c = c0 + c1 + c2 + c3;
+            uint32_t incl = c;
+#pragma unroll
+            for (int dd = 1; dd < 32; dd <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, dd);
+                if (lane >= dd) incl += v;
+            }
+            const uint32_t b0 = run + incl - c;
+            if (q < qb) wpre4[q] = make_uint4(b0, b0 + c0, b0 + c0 + c1, b0 + c0 + c1 + c2);
+            run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
     }
     __syncthreads();
     for (int e = tid; e < n; e += TOPK_THREADS) {
@@ -762,10 +820,8 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const float* row = scores + (long long)r * ld;
     const uint32_t got = __ldcg(w.cnt + r);
     if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
-        const int nw = (L + 31) / 32;
-        uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw);   // [nw] bitmap of selected indices
-        uint32_t* eqm = sel + nw;                                 // [nw] bitmap of keys equal to T
-        uint32_t* ekey = eqm + nw;                                // [cap]
+        uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem_raw);   // two bitmaps of the row
+        uint32_t* ekey = bitmaps + 2 * bitmap_words(L);               // [cap]
         int32_t* eidx = reinterpret_cast<int32_t*>(ekey + w.cap);
         const int n = (int)got;
         for (int base = 0; base < n; base += TOPK_THREADS * 8) {
@@ -787,7 +843,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
             }
         }
         __syncthreads();
-        select_entries(ekey, eidx, n, kk, L, sel, eqm, sh, o);
+        select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o);
         return;
     }
     select_streaming(row, L, kk, sh, o);
@@ -811,7 +867,7 @@ static int row_cap(int N_c, int k)
     return 2 * k + 2048 > 4096 ? 2 * k + 2048 : 4096;
 }
 
-static size_t row_smem_bytes(int N_c, int k) { return (size_t)row_cap(N_c, k) * 8 + (size_t)2 * ((N_c + 31) / 32) * 4; }
+static size_t row_smem_bytes(int N_c, int k) { return (size_t)row_cap(N_c, k) * 8 + (size_t)2 * bitmap_words(N_c) * 4; }
 
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k, int cap,
@@ -843,8 +899,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
     __syncthreads();
     const uint32_t n = n_cnt;
     if (n >= (uint32_t)kk && n <= (uint32_t)cap) {
-        const int nw = (L + 31) / 32;
-        select_entries(ekey, eidx, (int)n, kk, L, bitmaps, bitmaps + nw, sh, o);
+        select_entries(ekey, eidx, (int)n, kk, L, bitmaps, sh, o);
         return;
     }
     select_streaming(row, L, kk, sh, o);
@@ -896,13 +951,13 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
     }
     const LongRowWs w = lr_ws(ws, rows, k);
     topk_lr_sample_kernel<<<rows, TOPK_THREADS, 0, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w);
-    const size_t csmem = (size_t)w.cap * 8;
+    const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
     cudaFuncSetAttribute(topk_lr_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     topk_lr_collect_kernel<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
                                                                           p.n_chunks, w);
     // the fast route needs two bitmaps of the row and the entry list in
     // shared memory; shapes beyond that stream every row instead
-    size_t smem = (size_t)2 * ((N_c + 31) / 32) * 4 + (size_t)w.cap * 8;
+    size_t smem = (size_t)2 * bitmap_words(N_c) * 4 + (size_t)w.cap * 8;
     const int fast_ok = smem <= (size_t)200 * 1024;
     if (!fast_ok) smem = 0;
     cudaFuncSetAttribute(topk_lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
