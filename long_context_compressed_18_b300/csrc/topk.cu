@@ -11,8 +11,8 @@
 //
 // Rows up to 16,384 entries take one CTA each with all keys in shared memory;
 // rows up to TOPK_MAX_SINGLE take one fused CTA each (sampled threshold,
-// collection, select); longer rows take three kernels (sample, collect,
-// select) over many CTAs.
+// collection, select); longer rows take two kernels (collect with a sampled
+// threshold, select) over many CTAs.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -275,15 +275,15 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Long rows (more than one CTA's capacity): three kernels.
-//   sample   one CTA per row: keys of 4096 evenly spaced entries; a key at
-//            or below their key of rank ~2k * 4096 / L (plus a margin)
-//            becomes the row's collection threshold thr, expected to sit
-//            well below the k-th largest key;
-//   collect  one CTA per 16384-entry chunk: every entry with key >= thr is
-//            appended to the chunk's shared-memory list (4096 entries),
-//            whose slice of the row's entry list is then reserved with one
-//            global atomic;
+// Long rows (more than one CTA's capacity): the row counters are cleared, then
+// two kernels.
+//   collect  one CTA per 32768-entry chunk: from keys of 4096 evenly spaced
+//            entries of the row, every chunk CTA derives the same collection
+//            threshold thr -- a key at or below their key of rank
+//            ~2k * 4096 / L (plus a margin), expected to sit well below the
+//            k-th largest key -- then appends every entry of its chunk with
+//            key >= thr to a shared-memory list (4096 entries), whose slice
+//            of the row's entry list is reserved with one global atomic;
 //   select   one CTA per row: if the row collected at least k entries (so
 //            the k-th largest key T is >= thr and every entry with key >= T
 //            was collected) and no more than the list holds, the exact
@@ -295,15 +295,14 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
 //            compaction streaming the row from global memory.
 // Both routes give the exact result; only their speed depends on the data.
 // ---------------------------------------------------------------------------
-constexpr int LR_CHUNK = 16384;
+constexpr int LR_CHUNK = 32768;
 constexpr int LR_SAMPLES = 4096;
 constexpr int LR_LOCAL_CAP = 4096;   // a chunk's shared-memory list (32 KB: four CTAs an SM)
 
 static int lr_cap(int k) { return k * 4 > 8192 ? k * 4 : 8192; }
 
 struct LongRowWs {
-    uint32_t* thr;    // [rows] collection threshold (a key)
-    uint32_t* cnt;    // [rows] entries collected (may exceed cap)
+    uint32_t* cnt;    // [rows] entries collected (may exceed cap); cleared before the collection
     uint32_t* key;    // [rows][cap]
     int32_t* idx;     // [rows][cap]
     int cap;
@@ -316,8 +315,7 @@ static LongRowWs lr_ws(void* ws, int rows, int k)
     LongRowWs w;
     uint8_t* p = reinterpret_cast<uint8_t*>(ws);
     w.cap = lr_cap(k);
-    w.thr = reinterpret_cast<uint32_t*>(p);
-    w.cnt = w.thr + rows;
+    w.cnt = reinterpret_cast<uint32_t*>(p);
     p += lr_head_bytes(rows);
     w.key = reinterpret_cast<uint32_t*>(p);
     p += (size_t)rows * w.cap * 4;
@@ -458,20 +456,6 @@ __device__ uint32_t sample_threshold(const float* __restrict__ row, int L, int k
     return T;
 }
 
-__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_sample_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    LongRowWs w)
-{
-    __shared__ uint32_t keys[LR_SAMPLES];
-    __shared__ TopkShared sh;
-    const int r = blockIdx.x;
-    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
-    if (threadIdx.x == 0) w.cnt[r] = 0;
-    if (L <= k) return;                           // uniform: the row is copied whole
-    const uint32_t T = sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, keys, sh);
-    if (threadIdx.x == 0) w.thr[r] = T;
-}
-
 // The float whose key is k (inverse of score_key on keys of non-NaN values).
 __device__ __forceinline__ float key_value(uint32_t k)
 {
@@ -567,7 +551,7 @@ __device__ void collect_entries(const float* __restrict__ row, int c0, int len, 
     }
 }
 
-__global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
+__global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
     int n_chunks, LongRowWs w)
 {
@@ -576,6 +560,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     // matter to the select kernel)
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ uint32_t n_loc_s, base_s;
+    __shared__ TopkShared sh;
     uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [LR_LOCAL_CAP]
     int32_t* lidx = reinterpret_cast<int32_t*>(lkey + LR_LOCAL_CAP);
     const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
@@ -583,7 +568,10 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_collect_kernel(
     if (L <= k) return;
     const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
     if (len == 0) return;
-    const uint32_t thr = __ldcg(w.thr + r);
+    // every chunk CTA of the row derives the same threshold from the same
+    // samples (the list's storage holds the sample keys meanwhile)
+    static_assert(LR_LOCAL_CAP >= LR_SAMPLES, "sample keys live in the chunk list");
+    const uint32_t thr = sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, lkey, sh);
     if (threadIdx.x == 0) n_loc_s = 0;
     __syncthreads();
     const uint32_t cap = (uint32_t)w.cap;
@@ -950,7 +938,8 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
-    topk_lr_sample_kernel<<<rows, TOPK_THREADS, 0, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w);
+    cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)rows * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
     const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
     cudaFuncSetAttribute(topk_lr_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     topk_lr_collect_kernel<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
