@@ -81,8 +81,8 @@ typedef enum {
  *   out_scale   host array of n_streams device pointers (entries may be NULL
  *               for unscaled outputs); the array itself may be NULL.
  *   x, x_dtype, dim, out, out_dtype: host arrays of n_streams entries.
- * Requirements: 1 <= n_streams <= 4, m >= 1, dim[s] a multiple of 8 and at
- * most 512 (a multiple of 32 for CSA_E2M1).
+ * Requirements: 1 <= n_streams <= 4, m >= 1, dim[s] a power of two in
+ * [8, 256] (at least 32 for CSA_E2M1); otherwise CSA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_streams,
                           const void* const* x, const csa_dtype_t* x_dtype, const int* dim,
