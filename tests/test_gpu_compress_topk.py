@@ -208,8 +208,12 @@ def test_compress_tiles_stack_size():
 
 # ---- top-k on identical scores: bit-exact --------------------------------
 
-def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed, order=None):
+def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed, order=None, plant_inf=0):
     sc = inputs.random_scores(B * n_q, Nc, seed=seed, tie_levels=tie_levels)
+    if plant_inf:   # +inf and -inf at random entries of every row (ties among them go by index)
+        g = torch.Generator().manual_seed(seed + 1)
+        sc.scatter_(1, torch.randint(0, Nc, (B * n_q, plant_inf), generator=g), float("inf"))
+        sc.scatter_(1, torch.randint(0, Nc, (B * n_q, plant_inf), generator=g), float("-inf"))
     if order == "ascending":     # the best entries cluster at the end of the row
         sc = sc.sort(dim=1).values.contiguous()
     elif order == "descending":  # ... or at its start
@@ -244,6 +248,14 @@ def _topk_case(B, n_q, q_pos0, m, Nc, k, tie_levels, seed, order=None):
 ])
 def test_topk_bit_exact(case):
     _topk_case(seed=sum(case.values()) % 1000, **case)
+
+
+@pytest.mark.parametrize("Nc", [5000, 20000, 262144])
+def test_topk_infinite_scores(Nc):
+    """Rows holding +inf and -inf scores, for each row-length route (staged
+    keys, one fused CTA, chunked collection): infinities rank above and below
+    every finite score, equal ones by index."""
+    _topk_case(B=2, n_q=1, q_pos0=4 * Nc - 1, m=4, Nc=Nc, k=1024, tie_levels=0, seed=90, plant_inf=40)
 
 
 @pytest.mark.parametrize("order", ["ascending", "descending"])
