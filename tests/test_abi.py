@@ -58,3 +58,31 @@ def test_host_side_validation_without_gpu():
     # misaligned pointer
     st = L.swa_attn(1, 1, 0, 8, 4, 8, 64, 0.1, 8, 16, 16, lib.F32, 16, None, None)
     assert st == 3
+
+
+def test_empty_inputs_and_limits_without_gpu():
+    """Empty calls succeed without touching the device; the documented limits
+    are enforced on the host (fake, aligned device addresses are never used)."""
+    import ctypes as C
+    L = lib.load()
+    P, I = C.c_void_p, C.c_int
+    bf, e2 = (I * 1)(lib.BF16), (I * 1)(lib.E2M1)
+    addr = (P * 1)(256)
+    # compression: fewer tokens than one block, or no sequences, is an empty call
+    assert L.csa_compress(1, 3, 4, None, 1, (P * 1)(None), bf, (I * 1)(128), (P * 1)(None), bf, None, None) == 0
+    assert L.csa_compress(0, 64, 4, None, 1, (P * 1)(None), bf, (I * 1)(128), (P * 1)(None), bf, None, None) == 0
+    # widths: a power of two in [8, 256], at least 32 for E2M1 outputs
+    for d in (4, 24, 512):
+        st = L.csa_compress(1, 16, 4, 256, 1, addr, bf, (I * 1)(d), addr, bf, None, None)
+        assert st == 2 and "power of two" in L.csa_last_error().decode()
+    st = L.csa_compress(1, 16, 4, 256, 1, addr, bf, (I * 1)(16), addr, e2, addr, None)
+    assert st == 2 and "E2M1" in L.csa_last_error().decode()
+    # top-k: k <= 4096, rows <= 524,288 entries, long rows need the workspace
+    assert L.csa_topk_select(1, 1, 0, 4, 1000, 4097, 256, 256, None, 0, None) == 2
+    assert L.csa_topk_select(1, 1, 0, 4, 524289, 16, 256, 256, None, 0, None) == 2
+    need = L.csa_topk_select_workspace_size(2, 1, 262144, 1024)
+    st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, 256, None, 0, None)
+    assert st == 4 and str(need) in L.csa_last_error().decode()
+    st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, 256, 256, need - 16, None)
+    assert st == 4
+    assert L.csa_topk_select(0, 1, 0, 4, 1000, 16, None, None, None, 0, None) == 0
