@@ -378,9 +378,10 @@ def run_decode(args, torch, dist, rank, world):
         cpu = {"value": nq / tt, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{nq} of the 32 decode queries (full 262,144-entry caches), {tt:.1f} s"}
 
-    # indexer; top-k (sample, collect, select for rows past one CTA's capacity);
-    # attention (+ the slice combine when the key set is split)
-    launches_per_step = 1 + (3 if lib.csa_topk_select_workspace_size(B, 1, Nc, k) else 1) + \
+    # library kernels: indexer; top-k (collect and select for rows past one
+    # CTA's capacity, after a memset of the row counters that is not one of
+    # them); attention (+ the slice combine when the key set is split)
+    launches_per_step = 1 + (2 if lib.csa_topk_select_workspace_size(B, 1, Nc, k) else 1) + \
         (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
     res = {
         "metric": METRIC, "value": _job_rate(world, B * K, ms), "unit": "queries/s", "n_gpus": world,
