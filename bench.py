@@ -360,7 +360,7 @@ def run_decode(args, torch, dist, rank, world):
         "sparse_attn": B * (k * d * 2 * 2 + H * d * 2 * 2 + k * 4 + H * 4),
     }
     achieved = alg[dom] / (avg[dom] / 1e3) / 1e9
-    traffic = _traffic({"indexer": "indexer_tc_kernel", "topk": "topk_kernel", "sparse_attn": "attn_simt_kernel"}[dom],
+    traffic = _traffic({"indexer": "indexer_tc_kernel", "topk": "topk_lr_collect_kernel", "sparse_attn": "attn_tc_kernel"}[dom],
                        s.name)
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
