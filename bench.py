@@ -184,7 +184,6 @@ def _oracle_queries(s, x, bs, entry_stride=1):
 
 def run_decode(args, torch, dist, rank, world):
     from long_context_compressed_18_b300 import inputs, lib
-    import oracle  # noqa: F401  (cpu_baseline leg only)
 
     dev = torch.cuda.current_device()
     s = _decode_shape(args, rank)

@@ -121,7 +121,9 @@ csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, in
  * writes the first min(k, nv) indices in ascending order, padded with -1.
  * Exact radix selection on the fp32 bit patterns.
  *   scores   device fp32 [B, n_q, N_c];  topk  device int32 [B, n_q, k].
- * Requirements: 1 <= k <= 4096, N_c <= 524288.
+ * Requirements: 1 <= k <= 4096, N_c <= 524288, and B * n_q (times
+ * ceil(N_c / 32768) for rows longer than 32,768 entries) at most INT_MAX;
+ * otherwise CSA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */
 size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k);
 csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int k,
@@ -213,10 +215,32 @@ csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int 
  * csa_device_status -- synchronises the stream, then reads and clears this
  * device's status word: CSA_OK, CSA_ERR_TIMEOUT (a bounded device wait gave
  * up) or CSA_ERR_DEVICE (a device-side bounds check failed).
+ *   The status word is ONE word per device, shared by every call of this
+ *   library on every stream and host thread of the process: a flag raised by
+ *   a kernel on one stream is seen (and cleared) by csa_device_status on any
+ *   other stream of the same device.  Callers that run the library on
+ *   several streams at once and need per-stream attribution must serialise
+ *   the calls they check, or treat a non-OK status as a device-wide event.
  * csa_last_error -- message of the last non-OK status on this host thread.
  * ------------------------------------------------------------------------- */
 csa_status_t csa_device_status(csa_stream_t stream);
 const char* csa_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * csa_wait_selftest -- exercises the bounded waits every kernel of this
+ * library relies on (failure detection without a fault: a device wait that
+ * cannot complete gives up, records CSA_ERR_TIMEOUT in the status word and
+ * lets its CTA exit, leaving the context usable).  Launches one CTA whose
+ * first warp waits on an mbarrier that nothing completes, with a limit of
+ * limit_us microseconds (1 .. 2,000,000), and whose second warp waits on
+ * another such barrier until the first warp's timeout raises the CTA's abort
+ * flag.  No copy, MMA or tensor memory is in flight during the waits.
+ *   aborted  device uint32 (16-byte aligned): set to 1 if the second warp was
+ *            stopped by the abort flag (well before its own 2 s limit).
+ * Returns CSA_OK once launched; csa_device_status() then reports
+ * CSA_ERR_TIMEOUT.  The method's description has no counterpart of this call.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_wait_selftest(uint32_t limit_us, uint32_t* aborted, csa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -176,6 +176,36 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos
 namespace csa {
 // Sets the thread's last-error message for entry points defined in other files.
 csa_status_t report(csa_status_t st, const char* msg) { return fail(st, "%s", msg); }
+
+// Self-test of the bounded waits: warp 0 waits on an mbarrier that nothing
+// completes and gives up after limit_ns (flagging STATUS_TIMEOUT and the CTA's
+// abort flag); warp 1 waits on another such barrier under the default limit
+// and must stop as soon as the abort flag rises.  No copy, MMA or tensor
+// memory is involved, so nothing is in flight when the waits end.
+__global__ void wait_selftest_kernel(uint64_t limit_ns, unsigned* stopped_by_abort)
+{
+    __shared__ uint64_t bars[2];
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        if (warp == 0) {
+            mbar_wait_for(&bars[0], 0, &abort_flag, limit_ns);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            const bool ok = mbar_wait(&bars[1], 0, &abort_flag);
+            // stopped by the abort flag, well before its own 2 s limit
+            if (!ok && globaltimer_ns() - t0 < WAIT_LIMIT_NS / 2) atomicOr(stopped_by_abort, 1u);
+        }
+    }
+    __syncthreads();
+}
 }  // namespace csa
 
 // ---------------------------------------------------------------------------
@@ -307,6 +337,17 @@ extern "C" {
 
 const char* csa_last_error(void) { return g_msg; }
 
+csa_status_t csa_wait_selftest(uint32_t limit_us, uint32_t* aborted, csa_stream_t stream)
+{
+    if (limit_us < 1 || limit_us > 2000000u) return fail(CSA_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+    if (!aborted || !aligned16(aborted)) return fail(CSA_ERR_ALIGNMENT, "aborted NULL or not 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(aborted, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_status(e, "clear aborted flag");
+    wait_selftest_kernel<<<1, 64, 0, s>>>((uint64_t)limit_us * 1000ull, reinterpret_cast<unsigned*>(aborted));
+    return cuda_status(cudaGetLastError(), "wait self-test launch");
+}
+
 csa_status_t csa_device_status(csa_stream_t stream)
 {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
@@ -398,7 +439,7 @@ csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, in
 size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k)
 {
     if (B < 0 || n_q < 0 || N_c < 0 || k < 1) return 0;
-    return topk_workspace_bytes(B * n_q, N_c, k);
+    return topk_workspace_bytes((long long)B * n_q, N_c, k);
 }
 
 
@@ -408,10 +449,12 @@ csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int
     if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes");
     csa_status_t st = check_topk(N_c, k);
     if (st != CSA_OK) return st;
-    if ((long long)B * n_q == 0) return CSA_OK;
+    const long long rows = (long long)B * n_q;
+    if (rows == 0) return CSA_OK;
+    if (!topk_rows_ok(rows, N_c, k)) return fail(CSA_ERR_UNSUPPORTED, "top-k over %lld rows exceeds the grid limit", rows);
     if (!topk || !aligned16(topk) || (N_c > 0 && (!scores || !aligned16(scores))))
         return fail(CSA_ERR_ALIGNMENT, "scores/topk NULL or not aligned");
-    const size_t need = topk_workspace_bytes(B * n_q, N_c, k);
+    const size_t need = topk_workspace_bytes(rows, N_c, k);
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     return cuda_status(launch_topk(scores, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, workspace,
@@ -424,7 +467,7 @@ size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, 
     if (B < 0 || n_q < 0 || N_c < 0 || k < 1) return 0;
     const int rows = index_chunk_rows(B, n_q, N_c);
     return align_up((size_t)B * rows * N_c * 4, 256) + scores_ws_bytes(B, N_c, d_I, k_dtype) +
-           topk_workspace_bytes(B * rows, N_c, k);
+           topk_workspace_bytes((long long)B * rows, N_c, k);
 }
 
 csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
@@ -437,6 +480,8 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
     st = check_topk(N_c, k);
     if (st != CSA_OK) return st;
     if ((long long)B * n_q == 0) return CSA_OK;
+    if (!topk_rows_ok((long long)B * index_chunk_rows(B, n_q, N_c), N_c, k))
+        return fail(CSA_ERR_UNSUPPORTED, "top-k over %d sequences exceeds the grid limit", B);
     if (!topk || !aligned16(topk)) return fail(CSA_ERR_ALIGNMENT, "topk NULL or not aligned");
     const size_t need = csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))

@@ -75,22 +75,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// flags the status word) if it has not completed within WAIT_LIMIT_NS, or if
-// *abort becomes non-zero while waiting.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort = nullptr)
+// flags the status word) if it has not completed within limit_ns, or if
+// *abort becomes non-zero while waiting; a timeout also raises *abort so the
+// CTA's other waits stop too.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             flag_status(STATUS_TIMEOUT);
             if (abort) *abort = 1;
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort = nullptr)
+{
+    return mbar_wait_for(bar, parity, abort, WAIT_LIMIT_NS);
 }
 
 // ---------------------------------------------------------------------------

@@ -35,7 +35,9 @@ constexpr int TOPK_MAX_ROW = 524288;     // longest row (the select kernel's bit
 struct TopkPlan { int chunk; int n_chunks; };
 TopkPlan topk_plan(int N_c, int k);
 bool topk_supported(int N_c, int k);
-size_t topk_workspace_bytes(int rows, int N_c, int k);
+// rows * chunks of a long row fit one grid dimension (INT_MAX CTAs)
+bool topk_rows_ok(long long rows, int N_c, int k);
+size_t topk_workspace_bytes(long long rows, int N_c, int k);
 cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
                         cudaStream_t s);

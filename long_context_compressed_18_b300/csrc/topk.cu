@@ -13,6 +13,8 @@
 // rows up to TOPK_MAX_SINGLE take one fused CTA each (sampled threshold,
 // collection, select); longer rows take two kernels (collect with a sampled
 // threshold, select) over many CTAs.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -308,9 +310,9 @@ struct LongRowWs {
     int cap;
 };
 
-static size_t lr_head_bytes(int rows) { return ((size_t)rows * 8 + 255) / 256 * 256; }
+static size_t lr_head_bytes(long long rows) { return ((size_t)rows * 8 + 255) / 256 * 256; }
 
-static LongRowWs lr_ws(void* ws, int rows, int k)
+static LongRowWs lr_ws(void* ws, long long rows, int k)
 {
     LongRowWs w;
     uint8_t* p = reinterpret_cast<uint8_t*>(ws);
@@ -910,10 +912,17 @@ TopkPlan topk_plan(int N_c, int k)
 
 bool topk_supported(int N_c, int k) { return k >= 1 && k <= 4096 && N_c >= 0 && N_c <= TOPK_MAX_ROW; }
 
-size_t topk_workspace_bytes(int rows, int N_c, int k)
+bool topk_rows_ok(long long rows, int N_c, int k)
+{
+    // one CTA per row (times the chunks of a long row) in grid.x
+    const TopkPlan p = topk_plan(N_c, k);
+    return rows >= 0 && rows * p.n_chunks <= (long long)INT_MAX;
+}
+
+size_t topk_workspace_bytes(long long rows, int N_c, int k)
 {
     TopkPlan p = topk_plan(N_c, k);
-    if (p.n_chunks == 1) return 0;
+    if (p.n_chunks == 1 || rows <= 0) return 0;
     return lr_head_bytes(rows) + (size_t)rows * lr_cap(k) * 8;
 }
 
@@ -921,8 +930,10 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
                         cudaStream_t s)
 {
-    const int rows = B * n_q_rows;
-    if (rows == 0) return cudaSuccess;
+    const long long rows_ll = (long long)B * n_q_rows;
+    if (rows_ll == 0) return cudaSuccess;
+    if (!topk_rows_ok(rows_ll, N_c, k)) return cudaErrorInvalidConfiguration;   // callers check first
+    const int rows = (int)rows_ll;
     TopkPlan p = topk_plan(N_c, k);
     if (p.n_chunks == 1 && N_c <= TOPK_SMEM_ROW) {
         const size_t smem = (size_t)(N_c > 0 ? N_c : 1) * sizeof(uint32_t);

@@ -52,11 +52,13 @@ extern "C" csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, 
 {
     if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || q_pos0 < 0) return csa::report(CSA_ERR_INVALID_ARG, "bad sizes");
     if (!csa::topk_supported(N_c, k)) return csa::report(CSA_ERR_UNSUPPORTED, "top-k needs 1 <= k <= 4096, N_c <= 524288");
-    if ((long long)B * n_q == 0) return CSA_OK;
+    const long long rows = (long long)B * n_q;
+    if (rows == 0) return CSA_OK;
+    if (!csa::topk_rows_ok(rows, N_c, k)) return csa::report(CSA_ERR_UNSUPPORTED, "top-k row count exceeds the grid limit");
     if (!topk || (reinterpret_cast<uintptr_t>(topk) & 15u) ||
         (N_c > 0 && (!scores || (reinterpret_cast<uintptr_t>(scores) & 15u))))
         return csa::report(CSA_ERR_ALIGNMENT, "scores/topk NULL or not 16-byte aligned");
-    const size_t need = csa::topk_workspace_bytes(B * n_q, N_c, k);
+    const size_t need = csa::topk_workspace_bytes(rows, N_c, k);
     if (need > (size_t)CSA_TOPK_NOALLOC_SCRATCH_BYTES)
         return csa::report(CSA_ERR_WORKSPACE,
                            "selection needs more scratch than the built-in 4 MiB array "

@@ -24,7 +24,7 @@ EXPORTS = ("csa_compress", "csa_index_scores_workspace_size", "csa_index_scores"
            "csa_topk_select_workspace_size", "csa_topk_select", "csa_topk_select_noalloc",
            "csa_index_topk_workspace_size",
            "csa_index_topk", "csa_sparse_attn_workspace_size", "csa_sparse_attn", "hca_attn",
-           "swa_attn", "csa_device_status", "csa_last_error")
+           "swa_attn", "csa_device_status", "csa_last_error", "csa_wait_selftest")
 
 
 class CsaError(RuntimeError):
@@ -60,6 +60,7 @@ def load():
         "swa_attn": ([_I, _I, _L, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
         "csa_device_status": ([_P], _I),
         "csa_last_error": ([], C.c_char_p),
+        "csa_wait_selftest": ([C.c_uint32, _P, _P], _I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -169,6 +170,10 @@ def csa_device_status(stream=None):
 
 def csa_last_error() -> str:
     return load().csa_last_error().decode()
+
+
+def csa_wait_selftest(limit_us, aborted, stream=None):
+    _check(load().csa_wait_selftest(limit_us, _ptr(aborted), _stream(stream)))
 
 
 # ---- conveniences: dtype codes and output allocation (no compute) ---------

@@ -7,19 +7,22 @@ twice, so a capture can skip the first (cold) round; ``--time`` also prints
 CUDA-event timings of each case: 20 replays of a CUDA graph of the call, and
 20 eager calls.
 
-    python -m long_context_compressed_18_b300.profile_cases attn [--time]
-    python -m long_context_compressed_18_b300.profile_cases indexer [--time]
-    python -m long_context_compressed_18_b300.profile_cases topk [--time]
-    python -m long_context_compressed_18_b300.profile_cases compress [--time]
+    python profile_cases.py attn [--time]
+    python profile_cases.py indexer [--time]
+    python profile_cases.py topk [--time]
+    python profile_cases.py compress [--time]
 """
 from __future__ import annotations
 
 import argparse
 import math
+import os
+import sys
 
 import torch
 
-from . import inputs, lib
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from long_context_compressed_18_b300 import inputs, lib  # noqa: E402
 
 DEV = "cuda"
 

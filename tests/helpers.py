@@ -60,3 +60,56 @@ def topk_near_tie_check(gpu_sel, ora_sel, scores64, lens, k, rel=1e-3):
 def sync_status():
     torch.cuda.synchronize()
     lib.csa_device_status()
+
+
+def check_attn_stagewise(got_o, got_l, want_o, want_l, mag, what=""):
+    """Attention with BF16 I/O against the oracle run on identical inputs (the
+    same K/V values and the same selection).  Gates:
+      * max-abs 2e-2 (the spec's BF16 tolerance);
+      * per element, the error the arithmetic allows: the probabilities enter
+        the P.V product rounded to bf16 (relative 2^-9 each, at most
+        2^-9 * sum_j p_j |v_j| / l = 2^-9 * mag, mag being the same attention
+        over |V|) and the output is rounded to bf16 (2^-9 |o|); twice both;
+      * the normalised error max|got - want| / max|want| <= 1e-2, which still
+        bites where outputs are far below the absolute tolerance;
+      * lse within 5e-5 + 5e-6 relative, -inf exactly where the set is empty.
+    Returns the normalised error."""
+    g = np.asarray(got_o, np.float64).reshape(want_o.shape)
+    w = np.asarray(want_o, np.float64)
+    assert_close(g, w, atol=2e-2, what=f"{what} (spec max-abs)")
+    err = np.abs(g - w)
+    bound = 2.0 ** -8 * (np.abs(np.asarray(mag).reshape(w.shape)) + np.abs(w)) + 1e-6
+    assert np.all(err <= bound), f"{what}: worst excess over the per-element bound {np.max(err - bound):.3g}"
+    top = float(np.max(np.abs(w))) if w.size else 0.0
+    norm = float(err.max() / top) if top > 0 else 0.0
+    assert norm <= 1e-2, f"{what}: normalised error {norm:.3g}"
+    if got_l is not None:
+        gl = np.asarray(got_l, np.float64).reshape(want_l.shape)
+        fin = np.isfinite(want_l)
+        assert np.array_equal(np.isfinite(gl), fin) and np.all(gl[~fin] < 0), what
+        assert_close(gl[fin], want_l[fin], atol=5e-5, rtol=5e-6, what=f"{what} lse")
+    return norm
+
+
+def check_e2m1_keys(packed, sc_codes, x64):
+    """FP4 indexer keys from the compression epilogue against the oracle's
+    fp64 compressed values x64 [R, d]: each block scale lies within one E4M3
+    step of amax/6 (raised to the smallest positive E4M3), and each dequantised
+    element e * sc within half an E2M1 step (times sc) of x, or within
+    |x| - 6 sc where x / sc saturates.  Bit equality is not required: the GPU
+    quantises its fp32 compressed value, which may sit on the other side of a
+    rounding boundary from the fp64 one."""
+    vals = oracle.e2m1_decode_packed(packed).astype(np.float64)
+    sc = oracle.e4m3_decode(sc_codes).astype(np.float64)
+    R, d = x64.shape
+    nb = d // 32
+    xb = x64.reshape(R, nb, 32)
+    amax = np.abs(xb).max(-1)
+    target = np.maximum(amax / 6.0, 2.0 ** -9)
+    assert np.all(np.abs(sc - target) <= 2.0 ** -3 * target + 2.0 ** -10), "block scale off by more than one E4M3 step"
+    a = np.abs(xb) / sc[..., None]
+    half_step = np.where(a < 2, 0.25, np.where(a < 4, 0.5, 1.0)) * sc[..., None]
+    sat = np.maximum(np.abs(xb) - 6.0 * sc[..., None], 0.0)
+    bound = np.maximum(half_step, sat) * (1 + 1e-6) + 1e-6 * np.abs(xb) + 1e-9
+    err = np.abs(vals.reshape(R, nb, 32) - xb)
+    assert np.all(err <= bound), f"E2M1 element off: worst excess {np.max(err - bound):.3g}"

@@ -86,3 +86,18 @@ def test_empty_inputs_and_limits_without_gpu():
     st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, 256, 256, need - 16, None)
     assert st == 4
     assert L.csa_topk_select(0, 1, 0, 4, 1000, 16, None, None, None, 0, None) == 0
+
+
+def test_topk_row_count_is_checked_in_64_bits():
+    """B * n_q beyond INT_MAX (or beyond the grid once a long row is split into
+    chunks) is rejected on the host instead of wrapping around; the workspace
+    query computes in 64 bits."""
+    L = lib.load()
+    B, n_q = 70000, 40000                        # 2.8e9 rows
+    assert L.csa_topk_select(B, n_q, 0, 4, 1000, 16, 256, 256, None, 0, None) == 2
+    assert "grid limit" in L.csa_last_error().decode()
+    assert L.csa_topk_select_noalloc(B, n_q, 0, 4, 1000, 16, 256, 256, None) == 2
+    # 2^27 long rows of 16 chunks each exceed INT_MAX CTAs
+    assert L.csa_topk_select(1 << 14, 1 << 13, 4 * 524288 - 1, 4, 524288, 16, 256, 256, None, 0, None) == 2
+    need = L.csa_topk_select_workspace_size(65536, 65536, 262144, 1024)
+    assert need >= 65536 * 65536 * 8 * 4096      # no 32-bit wraparound

@@ -1,14 +1,23 @@
-"""End-to-end parity of the named workloads at their full sizes.
+"""Parity of the named workloads at their full sizes, in the launch
+configuration the benchmark times.
 
-The GPU runs every query; the oracle recomputes sampled query rows from the
-same seeded inputs (its own compression, quantisation, scores, top-k and
-attention -- nothing is taken from the GPU).  Gates:
-  * compressed K/V within one bf16 rounding of the oracle (all entries);
-  * top-k sets identical except at near-ties, |s - s_k| <= 1e-3 |s_k|;
-  * attention within max-abs 2e-2 on rows whose selected sets agree.
-Rows whose FP4 indexer keys straddle a quantisation boundary can differ in
-their sets beyond the near-tie band (a one-step code change, not a ranking
-error); those are counted and bounded separately."""
+Two modes (the oracle is the plain CPU implementation; nothing of it comes
+from the GPU except where a stage-wise gate says so):
+
+* stage-wise -- the gates.  Each GPU stage is compared with the oracle stage
+  fed the identical input bytes, including the GPU's own outputs of the stage
+  before: the oracle scores and selects on the GPU's compressed (and, for FP4,
+  quantised) indexer keys, and attends over the GPU's compressed K_c / V_c with
+  the GPU's own selection.  Top-k sets must be identical except at near-ties
+  (|s - s_k| <= 1e-3 |s_k|, counted), with no other exception; attention is
+  held to the per-element bound of the arithmetic and the normalised error
+  max|d| / max|ref| <= 1e-2.
+* end to end -- reported, and gated only where the spec's tolerances apply
+  unchanged: the oracle runs from the raw inputs (its own compression,
+  quantisation, scores, selection, attention).  Compressed K / V must agree to
+  within one bf16 rounding; top-k overlap is reported as recall; attention on
+  rows whose sets agree must meet max-abs 2e-2 (BF16 indexer) or 6e-2
+  (FP8 / FP4 indexer)."""
 import math
 
 import numpy as np
@@ -17,116 +26,172 @@ import torch
 
 import oracle
 from long_context_compressed_18_b300 import configs, inputs, pipeline
-from helpers import DEV, assert_close, host, sync_status, topk_near_tie_check
+from helpers import (DEV, assert_close, check_attn_stagewise, check_e2m1_keys, host, sync_status,
+                     topk_near_tie_check)
 
 pytestmark = pytest.mark.gpu
+
+# csa_index_topk scores the queries in chunks whose fp32 score buffer stays
+# within 256 MB: chunk rows = 2^28 / (4 * B * N_c), a multiple of 4.
+def _index_chunk_rows(s):
+    return max(4, ((1 << 28) // (4 * s.B * max(s.N_c, 1))) & ~3)
 
 
 def _np(t):
     return host(t).float().numpy()
 
 
-def _sample_rows(n_q, count, seed):
+def _sample_rows(n_q, count, seed, chunk=None, per_chunk=0):
+    """Sorted flat rows: the first, middle and last row, `count` random rows,
+    and with `chunk` given, `per_chunk` random rows inside every query chunk
+    of that size plus the rows on both sides of each chunk boundary."""
     rng = np.random.default_rng(seed)
-    fixed = [0, n_q - 1, n_q // 2]
-    extra = rng.choice(n_q, size=min(n_q, count), replace=False).tolist()
-    return np.array(sorted(set(fixed + extra)), np.int64)
+    picks = {0, n_q - 1, n_q // 2}
+    picks.update(rng.choice(n_q, size=min(n_q, count), replace=False).tolist())
+    if chunk:
+        for c0 in range(0, n_q, chunk):
+            c1 = min(n_q, c0 + chunk)
+            picks.update(rng.integers(c0, c1, size=per_chunk).tolist())
+            picks.update({c0, c1 - 1})
+    return np.array(sorted(picks), np.int64)
 
 
-def _oracle_csa_rows(s, x_cpu, rows):
-    """Oracle CSA for the given flat rows (batch 1 inputs on the host)."""
-    o = {}
-    kc = oracle.compress(x_cpu["logits"], x_cpu["k"], s.m)
-    vc = oracle.compress(x_cpu["logits"], x_cpu["v"], s.m)
-    ic = oracle.compress(x_cpu["logits"], x_cpu["idx_k"], s.m)
-    rnd = (lambda a: a.astype(np.float32)) if s.dtype == "f32" else \
-        (lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).float().numpy())
-    o["k_c64"], o["v_c64"] = kc, vc
-    kc32, vc32 = rnd(kc), rnd(vc)
+def _rnd(dtype):
+    if dtype == "f32":
+        return lambda a: np.asarray(a, np.float64).astype(np.float32)
+    return lambda a: torch.from_numpy(np.asarray(a, np.float64).astype(np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def _stagewise_csa(s, xc, g, rows):
+    """Stage-wise gates of one CSA layer on the sampled rows.  Returns
+    (near-tie rows, normalised attention error)."""
+    lens = oracle.visible(s.q_pos0 + rows % s.n_q, s.m, s.N_c)
+    # indexer + top-k on the GPU's compressed (quantised) indexer keys
+    s64, _, sel = oracle.csa_index_topk(xc["idx_q"], xc["idx_q_scale"], s.idx_q_dtype, host(g["idx_k_c"]),
+                                        host(g["idx_k_c_scale"]), s.idx_k_dtype, s.q_pos0, s.m, s.k, rows=rows)
+    gsel = host(g["topk"]).numpy().reshape(-1, s.k)[rows]
+    ties = topk_near_tie_check(gsel, sel, s64, lens, s.k)
+    # attention over the GPU's K_c / V_c with the GPU's own selection
+    q_rows = _np(xc["q"]).reshape(-1, s.H, s.d)[rows][None]
+    kc, vc = host(g["k_c"]), host(g["v_c"])
+    tau = 1.0 / math.sqrt(s.d)
+    want_o, want_l = oracle.attention(q_rows, kc, vc, tau, oracle.SPARSE, idx=gsel[None])
+    mag, _ = oracle.attention(q_rows, kc, np.abs(_np(vc)), tau, oracle.SPARSE, idx=gsel[None])
+    got_o = _np(g["out"]).reshape(-1, s.H, s.d)[rows]
+    got_l = host(g["lse"]).numpy().reshape(-1, s.H)[rows]
+    if s.dtype == "f32":
+        assert_close(got_o, want_o, atol=2e-5, rtol=2e-5, what="csa attention (fp32)")
+        assert_close(got_l, want_l, atol=5e-5, rtol=5e-6, what="csa lse (fp32)")
+        norm = 0.0
+    else:
+        norm = check_attn_stagewise(got_o, got_l, want_o, want_l, mag, what="csa attention")
+    return ties, norm
+
+
+def _end_to_end_csa(s, xc, g, rows, atol):
+    """The oracle from raw inputs on the sampled rows: gates compressed K / V
+    (one bf16 rounding), reports top-k recall, gates attention with the
+    spec's max-abs tolerance on rows whose sets agree.  Returns recall."""
+    kc = oracle.compress(xc["logits"], xc["k"], s.m)
+    vc = oracle.compress(xc["logits"], xc["v"], s.m)
+    ic = oracle.compress(xc["logits"], xc["idx_k"], s.m)
+    tol = dict(atol=1e-5, rtol=1e-5) if s.dtype == "f32" else dict(atol=1e-6, rtol=2.0 ** -8 + 1e-5)
+    assert_close(_np(g["k_c"]), kc, what="K_c", **tol)
+    assert_close(_np(g["v_c"]), vc, what="V_c", **tol)
     ic32 = ic.astype(np.float32)
     if s.idx_k_dtype == "e2m1":
+        check_e2m1_keys(host(g["idx_k_c"]).numpy().reshape(-1, s.d_I // 2),
+                        host(g["idx_k_c_scale"]).numpy().reshape(-1, s.d_I // 32), ic.reshape(-1, s.d_I))
         ik, iks = oracle.quant_e2m1_blocks(ic32)
     elif s.idx_k_dtype == "e4m3":
         ik, iks = oracle.quant_e4m3_rows(ic32)
     else:
-        ik, iks = rnd(ic), None
-    s64, s32, sel = oracle.csa_index_topk(x_cpu["idx_q"], x_cpu["idx_q_scale"], s.idx_q_dtype, ik, iks,
-                                          s.idx_k_dtype, s.q_pos0, s.m, s.k, rows=rows)
-    q_rows = _np(x_cpu["q"]).reshape(-1, s.H, s.d)[rows][None]
-    out, lse = oracle.attention(q_rows, kc32, vc32, 1.0 / math.sqrt(s.d), oracle.SPARSE, idx=sel[None])
-    o.update(scores64=s64, sel=sel, out=out, lse=lse)
-    return o
-
-
-def _compare_csa(s, g, o, rows, allow_quant_rows=0.0):
-    lens = oracle.visible(s.q_pos0 + rows, s.m, s.N_c)
+        assert_close(_np(g["idx_k_c"]), ic, what="indexer K_c", **tol)
+        ik, iks = _rnd(s.idx_k_dtype)(ic), None
+    _, _, sel = oracle.csa_index_topk(xc["idx_q"], xc["idx_q_scale"], s.idx_q_dtype, ik, iks, s.idx_k_dtype,
+                                      s.q_pos0, s.m, s.k, rows=rows)
     gsel = host(g["topk"]).numpy().reshape(-1, s.k)[rows]
-    try:
-        swaps = topk_near_tie_check(gsel, o["sel"], o["scores64"], lens, s.k)
-        quant_rows = 0
-    except AssertionError:
-        if allow_quant_rows == 0.0:
-            raise
-        swaps, quant_rows = 0, 0
-        for r in range(len(rows)):
-            try:
-                swaps += topk_near_tie_check(gsel[r:r + 1], o["sel"][r:r + 1], o["scores64"][r:r + 1], lens[r:r + 1], s.k)
-            except AssertionError:
-                quant_rows += 1
-        assert quant_rows <= allow_quant_rows * len(rows), (quant_rows, len(rows))
-    same = np.array([np.array_equal(gsel[r], o["sel"][r]) for r in range(len(rows))])
-    assert same.mean() >= 0.5, same.mean()
-    gout = _np(g["out"]).reshape(-1, s.H, s.d)[rows][same]
-    assert_close(gout, o["out"][same], atol=2e-2, what="csa attention")
-    return swaps, int((~same).sum())
+    lens = oracle.visible(s.q_pos0 + rows % s.n_q, s.m, s.N_c)
+    hit = sum(len(set(gsel[r][gsel[r] >= 0].tolist()) & set(sel[r][sel[r] >= 0].tolist())) for r in range(len(rows)))
+    recall = hit / max(1, int(np.minimum(lens, s.k).sum()))
+    same = np.array([np.array_equal(gsel[r], sel[r]) for r in range(len(rows))])
+    if same.any():
+        rnd = _rnd(s.dtype)
+        q_rows = _np(xc["q"]).reshape(-1, s.H, s.d)[rows[same]][None]
+        out, _ = oracle.attention(q_rows, rnd(kc), rnd(vc), 1.0 / math.sqrt(s.d), oracle.SPARSE,
+                                  idx=sel[same][None])
+        assert_close(_np(g["out"]).reshape(-1, s.H, s.d)[rows[same]], out, atol=atol, what="csa attention (e2e)")
+    return recall
+
+
+def _run_csa_layer(s, rows_count, seed, per_chunk=0):
+    x = inputs.make_inputs(s, device=DEV)
+    g = pipeline.csa_layer(x, s, pipeline.Workspace())
+    sync_status()
+    xc = {k: (None if v is None else v.cpu()) for k, v in x.items()}
+    chunk = _index_chunk_rows(s) if per_chunk else None
+    rows = _sample_rows(s.B * s.n_q, rows_count, seed, chunk=chunk, per_chunk=per_chunk)
+    ties, norm = _stagewise_csa(s, xc, g, rows)
+    atol = 6e-2 if s.idx_k_dtype in ("e4m3", "e2m1") else 2e-2
+    recall = _end_to_end_csa(s, xc, g, rows, atol)
+    print(f"{s.name}: {len(rows)} rows, near-tie rows {ties}, attention normalised error {norm:.2e}, "
+          f"end-to-end top-k recall {recall:.4f}")
+    return ties, recall
 
 
 def test_tiny_csa_f32_full():
     s = configs.TINY_CSA_F32
     x = inputs.make_inputs(s)
-    ws = pipeline.Workspace()
-    g = pipeline.csa_layer({k: (None if v is None else v.to(DEV)) for k, v in x.items()}, s, ws)
+    g = pipeline.csa_layer({k: (None if v is None else v.to(DEV)) for k, v in x.items()}, s, pipeline.Workspace())
     sync_status()
     rows = np.arange(s.n_q)
-    o = _oracle_csa_rows(s, x, rows)
-    assert_close(_np(g["k_c"]), o["k_c64"], atol=1e-5, rtol=1e-5, what="K_c")
-    assert_close(_np(g["v_c"]), o["v_c64"], atol=1e-5, rtol=1e-5, what="V_c")
-    swaps, diff_rows = _compare_csa(s, g, o, rows)
-    assert diff_rows <= 0.01 * s.n_q
-    assert_close(_np(g["out"]).reshape(-1, s.H, s.d), o["out"], atol=1e-4, what="all rows") if diff_rows == 0 else None
+    ties, _ = _stagewise_csa(s, x, g, rows)          # every row
+    recall = _end_to_end_csa(s, x, g, rows, atol=2e-2)
+    assert recall >= 0.99, recall
 
 
 def test_csa_prefill_bf16_full_size():
     s = configs.CSA_PREFILL_BF16
-    x = inputs.make_inputs(s, device=DEV)
-    ws = pipeline.Workspace()
-    g = pipeline.csa_layer(x, s, ws)
-    sync_status()
-    xc = {k: (None if v is None else v.cpu()) for k, v in x.items()}
-    rows = _sample_rows(s.n_q, 24, seed=2)
-    o = _oracle_csa_rows(s, xc, rows)
-    assert_close(_np(g["k_c"]), o["k_c64"], atol=1e-6, rtol=2.0 ** -8 + 1e-5, what="K_c")
-    assert_close(_np(g["v_c"]), o["v_c64"], atol=1e-6, rtol=2.0 ** -8 + 1e-5, what="V_c")
-    _compare_csa(s, g, o, rows)
+    _, recall = _run_csa_layer(s, 48, seed=2, per_chunk=4)
+    assert recall >= 0.95, recall
+
+
+@pytest.mark.parametrize("layer", [2, 4])
+def test_hybrid_stack_csa_layer_stagewise(layer):
+    """A CSA layer of the hybrid stack at n = 131,072 (FP4 indexer keys from
+    the compression epilogue, widened to E4M3 for the tcgen05 indexer): the
+    oracle widens and scores the GPU's own E2M1 keys and block scales; sampled
+    rows cover every csa_index_topk query chunk and both sides of its
+    boundaries."""
+    s = configs.STACK_LAYERS[layer]
+    assert s.kind == "csa" and s.idx_k_dtype == "e2m1"
+    _, recall = _run_csa_layer(s, 16, seed=10 + layer, per_chunk=1)
+    assert recall >= 0.9, recall
 
 
 def test_csa_decode_1m_full_size():
+    """Every one of the 32 sequences: top-k against the oracle's selection on
+    the same E4M3 cache (near-ties only), attention and lse against the oracle
+    on the GPU's own selection."""
     s = configs.CSA_DECODE_1M
     x = inputs.make_inputs(s, device=DEV)
-    ws = pipeline.Workspace()
-    g = pipeline.csa_decode(x, s, ws)
+    g = pipeline.csa_decode(x, s, pipeline.Workspace())
     sync_status()
-    for b in (0, 13, 31):
+    gsel_all = host(g["topk"]).numpy().reshape(s.B, s.k)
+    tau = 1.0 / math.sqrt(s.d)
+    ties = 0
+    for b in range(s.B):
         iq, iqs = x["idx_q"][b:b + 1].cpu(), x["idx_q_scale"][b:b + 1].cpu()
         ik, iks = x["idx_k_c"][b:b + 1].cpu(), x["idx_k_c_scale"][b:b + 1].cpu()
-        s64, s32, sel = oracle.csa_index_topk(iq, iqs, "e4m3", ik, iks, "e4m3", s.q_pos0, s.m, s.k)
-        gsel = host(g["topk"][b]).numpy().reshape(1, s.k)
-        topk_near_tie_check(gsel, sel, s64, [s.N_c], s.k)
-        if np.array_equal(gsel, sel):
-            out, lse = oracle.attention(x["q"][b:b + 1].cpu(), x["k_c"][b:b + 1].cpu(), x["v_c"][b:b + 1].cpu(),
-                                        1.0 / math.sqrt(s.d), oracle.SPARSE, idx=sel[None])
-            assert_close(_np(g["out"][b]).reshape(1, s.H, s.d), out, atol=2e-2, what=f"decode attn b={b}")
-            assert_close(host(g["lse"][b]).numpy().reshape(1, s.H), lse, atol=1e-3, what="decode lse")
+        s64, _, sel = oracle.csa_index_topk(iq, iqs, "e4m3", ik, iks, "e4m3", s.q_pos0, s.m, s.k)
+        gsel = gsel_all[b:b + 1]
+        ties += topk_near_tie_check(gsel, sel, s64, [s.N_c], s.k)
+        q, kc, vc = x["q"][b:b + 1].cpu(), x["k_c"][b:b + 1].cpu(), x["v_c"][b:b + 1].cpu()
+        want_o, want_l = oracle.attention(q, kc, vc, tau, oracle.SPARSE, idx=gsel[None])
+        mag, _ = oracle.attention(q, kc, vc.float().abs(), tau, oracle.SPARSE, idx=gsel[None])
+        check_attn_stagewise(_np(g["out"][b]).reshape(1, s.H, s.d), host(g["lse"][b]).numpy().reshape(1, s.H),
+                             want_o, want_l, mag, what=f"decode b={b}")
+    print(f"decode: 32 sequences, near-tie rows {ties}")
 
 
 def test_hca_prefill_1m_full_size():
@@ -138,42 +203,50 @@ def test_hca_prefill_1m_full_size():
     kc = oracle.compress(xc["logits"], xc["k"], s.m)
     vc = oracle.compress(xc["logits"], xc["v"], s.m)
     assert_close(_np(g["k_c"]), kc, atol=1e-6, rtol=2.0 ** -8 + 1e-5, what="K_c")
+    assert_close(_np(g["v_c"]), vc, atol=1e-6, rtol=2.0 ** -8 + 1e-5, what="V_c")
     rows = _sample_rows(s.n_q, 12, seed=4)
-    rnd = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    # stage-wise: attention over the GPU's own K_c / V_c
     q_rows = _np(xc["q"]).reshape(-1, s.H, s.d)[rows]
-    want = np.concatenate([
-        oracle.attention(q_rows[i:i + 1][None], rnd(kc), rnd(vc), 1.0 / math.sqrt(s.d), oracle.CLOSED_BLOCKS,
-                         q_pos0=s.q_pos0 + int(r), m=s.m)[0]
-        for i, r in enumerate(rows)])
-    assert_close(_np(g["out"]).reshape(-1, s.H, s.d)[rows], want, atol=2e-2, what="hca attention")
+    gk, gv = host(g["k_c"]), host(g["v_c"])
+    tau = 1.0 / math.sqrt(s.d)
+    want, wl, mag = [], [], []
+    for i, r in enumerate(rows):
+        o, l_ = oracle.attention(q_rows[i:i + 1][None], gk, gv, tau, oracle.CLOSED_BLOCKS, q_pos0=s.q_pos0 + int(r), m=s.m)
+        mg, _ = oracle.attention(q_rows[i:i + 1][None], gk, np.abs(_np(gv)), tau, oracle.CLOSED_BLOCKS,
+                                 q_pos0=s.q_pos0 + int(r), m=s.m)
+        want.append(o), wl.append(l_), mag.append(mg)
+    check_attn_stagewise(_np(g["out"]).reshape(-1, s.H, s.d)[rows], host(g["lse"]).numpy().reshape(-1, s.H)[rows],
+                         np.concatenate(want), np.concatenate(wl), np.concatenate(mag), what="hca attention")
 
 
 def test_hybrid_stack_full_size():
+    """All six layers of the stack end to end at n = 131,072 on sampled rows:
+    SWA and HCA stage-wise (HCA over the GPU's own compressed K / V); the CSA
+    layers' stage-wise gates are in test_hybrid_stack_csa_layer_stagewise."""
     ws = pipeline.Workspace()
     for li, s in enumerate(configs.STACK_LAYERS):
+        if s.kind == "csa":
+            continue
         x = inputs.make_inputs(s, device=DEV)
         g = pipeline.run_layer(x, s, ws)
         sync_status()
         rows = _sample_rows(s.n_q, 6, seed=10 + li)
         xc = {k: (None if v is None else v.cpu()) for k, v in x.items()}
-        if s.kind == "csa":
-            o = _oracle_csa_rows(s, xc, rows)
-            _compare_csa(s, g, o, rows, allow_quant_rows=0.34)
-        elif s.kind == "hca":
-            rnd = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).float().numpy()
-            kc = rnd(oracle.compress(xc["logits"], xc["k"], s.m))
-            vc = rnd(oracle.compress(xc["logits"], xc["v"], s.m))
-            q_rows = _np(xc["q"]).reshape(-1, s.H, s.d)[rows]
-            want = np.concatenate([
-                oracle.attention(q_rows[i:i + 1][None], kc, vc, 1.0 / math.sqrt(s.d), oracle.CLOSED_BLOCKS,
-                                 q_pos0=int(r), m=s.m)[0] for i, r in enumerate(rows)])
-            assert_close(_np(g["out"]).reshape(-1, s.H, s.d)[rows], want, atol=2e-2, what=f"layer {li} hca")
+        q_rows = _np(xc["q"]).reshape(-1, s.H, s.d)[rows]
+        tau = 1.0 / math.sqrt(s.d)
+        if s.kind == "hca":
+            kc = oracle.compress(xc["logits"], xc["k"], s.m)
+            assert_close(_np(g["k_c"]), kc, atol=1e-6, rtol=2.0 ** -8 + 1e-5, what=f"layer {li} K_c")
+            K, V = host(g["k_c"]), host(g["v_c"])
+            kw = lambda r: dict(mode=oracle.CLOSED_BLOCKS, q_pos0=int(r), m=s.m)
         else:
-            q_rows = _np(xc["q"]).reshape(-1, s.H, s.d)[rows]
-            want = np.concatenate([
-                oracle.attention(q_rows[i:i + 1][None], xc["k"], xc["v"], 1.0 / math.sqrt(s.d), oracle.WINDOW,
-                                 q_pos0=int(r), window=s.window)[0] for i, r in enumerate(rows)])
-            assert_close(_np(g["out"]).reshape(-1, s.H, s.d)[rows], want, atol=2e-2, what=f"layer {li} swa")
+            K, V = xc["k"], xc["v"]
+            kw = lambda r: dict(mode=oracle.WINDOW, q_pos0=int(r), window=s.window)
+        res = [oracle.attention(q_rows[i:i + 1][None], K, V, tau, **kw(r)) for i, r in enumerate(rows)]
+        mag = [oracle.attention(q_rows[i:i + 1][None], K, np.abs(_np(V)), tau, **kw(r))[0] for i, r in enumerate(rows)]
+        check_attn_stagewise(_np(g["out"]).reshape(-1, s.H, s.d)[rows], host(g["lse"]).numpy().reshape(-1, s.H)[rows],
+                             np.concatenate([o for o, _ in res]), np.concatenate([l_ for _, l_ in res]),
+                             np.concatenate(mag), what=f"layer {li} {s.kind}")
         del x, g, xc
         torch.cuda.empty_cache()
 
