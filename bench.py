@@ -189,11 +189,10 @@ def run_decode(args, torch, dist, rank, world):
     s = _decode_shape(args, rank)
     B, Nc, k, HI, dI, H, d = s.B, s.N_c, s.k, s.H_I, s.d_I, s.H, s.d
     x = inputs.make_inputs(s, device="cuda")
-    scores = torch.empty(B, 1, Nc, dtype=torch.float32, device="cuda")
     topk = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
     out = torch.empty(B, 1, H, d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, 1, H, dtype=torch.float32, device="cuda")
-    ws_t_b = lib.csa_topk_select_workspace_size(B, 1, Nc, k)
+    ws_t_b = lib.csa_index_topk_workspace_size(B, 1, Nc, HI, dI, k, lib.E4M3)
     ws_a_b = lib.csa_sparse_attn_workspace_size(B, 1, H, d, k)
     ws_t = lib.empty_workspace(ws_t_b)
     ws_a = lib.empty_workspace(ws_a_b)
@@ -201,19 +200,19 @@ def run_decode(args, torch, dist, rank, world):
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
+        # Lightning Indexer + top-k in one call (the indexer kernel collects
+        # each row's candidates; a select kernel finishes the selection), then
+        # sparse attention
         if ev:
             ev[0].record(stream)
-        lib.csa_index_scores(B, 1, s.q_pos0, s.m, Nc, HI, dI, x["idx_q"], lib.E4M3, x["idx_q_scale"],
-                             x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], scores)
+        lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, x["idx_q"], lib.E4M3, x["idx_q_scale"],
+                           x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], topk, ws_t, ws_t_b)
         if ev:
             ev[1].record(stream)
-        lib.csa_topk_select(B, 1, s.q_pos0, s.m, Nc, k, scores, topk, ws_t, ws_t_b)
-        if ev:
-            ev[2].record(stream)
         lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, x["q"], x["k_c"], x["v_c"], lib.BF16, topk, out, lse,
                             ws_a, ws_a_b)
         if ev:
-            ev[3].record(stream)
+            ev[2].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -222,16 +221,15 @@ def run_decode(args, torch, dist, rank, world):
 
     # ---- per-call breakdown: eager steps with CUDA events around each call ----
     KE = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(KE)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(KE)]
     for i in range(KE):
         step(evs[i])
     torch.cuda.synchronize()
     lib.csa_device_status()
-    per = {"indexer": [], "topk": [], "sparse_attn": []}
+    per = {"index_topk": [], "sparse_attn": []}
     for e in evs:
-        per["indexer"].append(e[0].elapsed_time(e[1]))
-        per["topk"].append(e[1].elapsed_time(e[2]))
-        per["sparse_attn"].append(e[2].elapsed_time(e[3]))
+        per["index_topk"].append(e[0].elapsed_time(e[1]))
+        per["sparse_attn"].append(e[1].elapsed_time(e[2]))
 
     # ---- timed region: K replays of a CUDA graph of one whole step ----
     graph = torch.cuda.CUDAGraph()
@@ -315,9 +313,8 @@ def run_decode(args, torch, dist, rank, world):
             stream.wait_event(up_done[j])
             if used[j]:
                 stream.wait_event(down_done[j])           # step i-2's results have left these buffers
-            lib.csa_index_scores(B, 1, s.q_pos0, s.m, Nc, HI, dI, di["idx_q"], lib.E4M3, di["idx_q_scale"],
-                                 x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], scores)
-            lib.csa_topk_select(B, 1, s.q_pos0, s.m, Nc, k, scores, do["topk"], ws_t, ws_t_b)
+            lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, di["idx_q"], lib.E4M3, di["idx_q_scale"],
+                               x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], do["topk"], ws_t, ws_t_b)
             lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, di["q"], x["k_c"], x["v_c"], lib.BF16, do["topk"],
                                 do["out"], do["lse"], ws_a, ws_a_b)
             comp_done[j].record(stream)
@@ -353,14 +350,14 @@ def run_decode(args, torch, dist, rank, world):
     peaks, peak_src = _peaks()
     avg = {kk: statistics.mean(v) for kk, v in per.items()}
     dom = max(avg, key=avg.get)
-    alg = {  # algorithmic bytes per launch
-        "indexer": B * (Nc * (dI + 4) + HI * (dI + 4)),
-        "topk": B * Nc * 4,
+    alg = {  # algorithmic bytes per call: what the call must read and write at least
+        # keys + row scales, the query and its head scales, the top-k indices
+        # (the scores are an intermediate of the fused call)
+        "index_topk": B * (Nc * (dI + 4) + HI * (dI + 4) + k * 4),
         "sparse_attn": B * (k * d * 2 * 2 + H * d * 2 * 2 + k * 4 + H * 4),
     }
     achieved = alg[dom] / (avg[dom] / 1e3) / 1e9
-    traffic = _traffic({"indexer": "indexer_tc_kernel", "topk": "topk_lr_collect_kernel", "sparse_attn": "attn_tc_kernel"}[dom],
-                       s.name)
+    traffic = _traffic({"index_topk": "indexer_tc_kernel", "sparse_attn": "attn_tc_kernel"}[dom], s.name)
     roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
             "peak_source": peak_src, "algorithmic_bytes_per_launch": alg[dom],
@@ -377,11 +374,10 @@ def run_decode(args, torch, dist, rank, world):
         cpu = {"value": nq / tt, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{nq} of the 32 decode queries (full 262,144-entry caches), {tt:.1f} s"}
 
-    # library kernels: indexer; top-k (collect and select for rows past one
-    # CTA's capacity, after a memset of the row counters that is not one of
-    # them); attention (+ the slice combine when the key set is split)
-    launches_per_step = 1 + (2 if lib.csa_topk_select_workspace_size(B, 1, Nc, k) else 1) + \
-        (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
+    # library kernels: the collecting indexer and the select (after a memset
+    # of the row counters that is not one of them); attention (+ the slice
+    # combine when the key set is split)
+    launches_per_step = 2 + (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
     res = {
         "metric": METRIC, "value": _job_rate(world, B * K, ms), "unit": "queries/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -390,7 +386,8 @@ def run_decode(args, torch, dist, rank, world):
         "config": {"workload": s.name, "batch_per_gpu": B, "ctx_tokens": s.n, "compressed_entries": Nc,
                    "indexer": f"{HI}x{dI} e4m3", "top_k": k, "attention": f"{H}x{d} bf16",
                    "l2": "inputs (5.2 GB per GPU) exceed L2; no flush",
-                   "launch": "one step (indexer, top-k, sparse attention) captured in a CUDA graph and replayed",
+                   "launch": "one step (indexer with fused top-k collection, select, sparse attention) captured "
+                             "in a CUDA graph and replayed",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * K,

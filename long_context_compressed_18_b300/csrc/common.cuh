@@ -333,6 +333,16 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt
            | ((M >> 4) << 24);             // M / 16
 }
 
+// Order-preserving 32-bit key of an fp32 score for radix selection: larger
+// score, larger key; -0 folded onto +0; NaN ranks below everything (key 0).
+__device__ __forceinline__ uint32_t score_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0u) u = 0u;                               // -0 -> +0
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0u;           // NaN ranks last
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // ---------------------------------------------------------------------------
 // Conversions
 // ---------------------------------------------------------------------------

@@ -23,14 +23,6 @@ namespace csa {
 constexpr int TOPK_THREADS = 512;
 constexpr int TOPK_WARPS = TOPK_THREADS / 32;
 
-__device__ __forceinline__ uint32_t score_key(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    if ((u << 1) == 0u) u = 0u;                               // -0 -> +0
-    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0u;           // NaN ranks last
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Radix levels over the 32-bit key: bits 31..21 (2048 bins), 20..10 (2048),
 // 9..0 (1024).  The first level's histogram is built while the scores are
 // loaded; the second while the elements of the selected first-level bin are
@@ -303,12 +295,7 @@ constexpr int LR_LOCAL_CAP = 4096;   // a chunk's shared-memory list (32 KB: fou
 
 static int lr_cap(int k) { return k * 4 > 8192 ? k * 4 : 8192; }
 
-struct LongRowWs {
-    uint32_t* cnt;    // [rows] entries collected (may exceed cap); cleared before the collection
-    uint32_t* key;    // [rows][cap]
-    int32_t* idx;     // [rows][cap]
-    int cap;
-};
+using LongRowWs = TopkLists;
 
 static size_t lr_head_bytes(long long rows) { return ((size_t)rows * 8 + 255) / 256 * 256; }
 
@@ -318,6 +305,7 @@ static LongRowWs lr_ws(void* ws, long long rows, int k)
     uint8_t* p = reinterpret_cast<uint8_t*>(ws);
     w.cap = lr_cap(k);
     w.cnt = reinterpret_cast<uint32_t*>(p);
+    w.floor = w.cnt + rows;
     p += lr_head_bytes(rows);
     w.key = reinterpret_cast<uint32_t*>(p);
     p += (size_t)rows * w.cap * 4;
@@ -606,8 +594,15 @@ __host__ __device__ constexpr int bitmap_words(int L) { return (((L + 31) / 32) 
 // n >= kk) -- the top kk by (score desc, index asc) -- written to o in
 // ascending index order.  bitmaps: shared memory for two bitmaps of
 // bitmap_words(L) words each (16-byte aligned).
-__device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* bitmaps,
-                               TopkShared& sh, int32_t* __restrict__ o)
+//
+// need: the largest threshold any producer of the list collected at (0 when
+// the list holds every entry at or above one threshold).  The list is then
+// complete only if the k-th largest key among its entries is at least need
+// (every entry of the row at or above that key was collected); otherwise
+// nothing is written and false is returned, for the caller to select by
+// streaming the row.
+__device__ bool select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* bitmaps,
+                               TopkShared& sh, int32_t* __restrict__ o, uint32_t need = 0u)
 {
     const int tid = threadIdx.x;
     const int nw = (L + 31) / 32, nw4 = bitmap_words(L);
@@ -653,6 +648,8 @@ __device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int k
     int teq;
     radix_threshold(ekey, n, kk, sh, T, teq, &n_eq);
     __syncthreads();
+    // T is the spread key of a collected entry: its key is lo + (T >> shl)
+    if (lo + (T >> shl) < need) return false;   // uniform: every thread holds the same T
     // mark the selection; keys equal to T join it directly unless only some
     // of them are taken (then the first teq in index order, below)
     const bool all_eq = n_eq == (uint32_t)teq;
@@ -751,6 +748,7 @@ __device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int k
             if (pos < (uint32_t)kk) o[pos] = j;
         }
     }
+    return true;
 }
 
 // Exact selection of a row's top kk streamed from global memory: the three
@@ -791,7 +789,7 @@ __device__ void select_streaming(const float* __restrict__ row, int L, int kk, T
 
 __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
+    LongRowWs w, int fast_ok, int use_floor, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
@@ -833,8 +831,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
             }
         }
         __syncthreads();
-        select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o);
-        return;
+        const uint32_t need = use_floor ? __ldcg(w.floor + r) : 0u;
+        if (select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o, need)) return;
+        __syncthreads();
     }
     select_streaming(row, L, kk, sh, o);
 }
@@ -926,6 +925,22 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k)
     return lr_head_bytes(rows) + (size_t)rows * lr_cap(k) * 8;
 }
 
+// The select kernel over a row's entry list.  The fast route needs two
+// bitmaps of the row and the entry list in shared memory; shapes beyond that
+// stream every row instead.
+static cudaError_t launch_select(const float* scores, long long ld, int n_q_rows, long long q_pos0, int m, int N_c,
+                                 int k, const LongRowWs& w, int rows, int use_floor, int32_t* out,
+                                 long long out_b_stride, cudaStream_t s)
+{
+    size_t smem = (size_t)2 * bitmap_words(N_c) * 4 + (size_t)w.cap * 8;
+    const int fast_ok = smem <= (size_t)200 * 1024;
+    if (!fast_ok) smem = 0;
+    cudaFuncSetAttribute(topk_lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    topk_lr_select_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok,
+                                                          use_floor, out, out_b_stride);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
                         cudaStream_t s)
@@ -949,21 +964,33 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
-    cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)rows * sizeof(uint32_t), s);
+    cudaError_t e = launch_topk_clear_lists(w, rows, s);
     if (e != cudaSuccess) return e;
     const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
     cudaFuncSetAttribute(topk_lr_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     topk_lr_collect_kernel<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
                                                                           p.n_chunks, w);
-    // the fast route needs two bitmaps of the row and the entry list in
-    // shared memory; shapes beyond that stream every row instead
-    size_t smem = (size_t)2 * bitmap_words(N_c) * 4 + (size_t)w.cap * 8;
-    const int fast_ok = smem <= (size_t)200 * 1024;
-    if (!fast_ok) smem = 0;
-    cudaFuncSetAttribute(topk_lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    topk_lr_select_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok,
-                                                          out, out_b_stride);
-    return cudaGetLastError();
+    return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, rows, 0, out, out_b_stride, s);
+}
+
+TopkLists topk_lists(void* ws, long long rows, int k) { return lr_ws(ws, rows, k); }
+
+bool topk_long_rows(int N_c, int k) { return topk_plan(N_c, k).n_chunks > 1; }
+
+cudaError_t launch_topk_clear_lists(const TopkLists& w, long long rows, cudaStream_t s)
+{
+    // the counters and the collection floors (adjacent)
+    return cudaMemsetAsync(w.cnt, 0, (size_t)rows * 2 * sizeof(uint32_t), s);
+}
+
+cudaError_t launch_topk_select_lists(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0, int m,
+                                     int N_c, int k, int32_t* out, long long out_b_stride, void* ws, cudaStream_t s)
+{
+    const long long rows = (long long)B * n_q_rows;
+    if (rows == 0) return cudaSuccess;
+    if (!topk_rows_ok(rows, N_c, k)) return cudaErrorInvalidConfiguration;
+    return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, lr_ws(ws, rows, k), (int)rows, 1, out,
+                         out_b_stride, s);
 }
 
 }  // namespace csa

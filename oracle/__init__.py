@@ -244,12 +244,26 @@ def csa_index_topk(idx_q, idx_q_scale, q_kind, idx_k, idx_k_scale, k_kind,
         kv, ks = e4m3_decode(idx_k), _np(idx_k_scale, np.float32)
     else:
         kv, ks = _np(idx_k, np.float32), None
-    qv = e4m3_decode(idx_q) if q_kind == "e4m3" else _np(idx_q, np.float32)
-    qs = None if idx_q_scale is None else _np(idx_q_scale, np.float32)
-    B, n_q = qv.shape[:2]
+    B, n_q = idx_q.shape[:2]
     Nc = kv.shape[1]
-    s64, s32 = index_scores(qv, qs, kv, ks, q_pos0, m, rows)
-    flat = np.arange(B * n_q) if rows is None else _np(rows, np.int64)
+    if rows is None:
+        qv = e4m3_decode(idx_q) if q_kind == "e4m3" else _np(idx_q, np.float32)
+        qs = None if idx_q_scale is None else _np(idx_q_scale, np.float32)
+        s64, s32 = index_scores(qv, qs, kv, ks, q_pos0, m)
+        flat = np.arange(B * n_q)
+    else:
+        # only the requested rows' queries are decoded: each row is scored as
+        # a batch of one at its own position, against its sequence's keys
+        flat = _np(rows, np.int64)
+        s64 = np.empty((flat.size, Nc), np.float64)
+        s32 = np.empty((flat.size, Nc), np.float32)
+        for r, f in enumerate(flat):
+            b, i = int(f) // n_q, int(f) % n_q
+            q1 = idx_q[b:b + 1, i:i + 1]
+            qv = e4m3_decode(q1) if q_kind == "e4m3" else _np(q1, np.float32)
+            qs = None if idx_q_scale is None else _np(idx_q_scale[b:b + 1, i:i + 1], np.float32)
+            ks1 = None if ks is None else ks[b:b + 1]
+            s64[r:r + 1], s32[r:r + 1] = index_scores(qv, qs, kv[b:b + 1], ks1, q_pos0 + i, m)
     lens = visible(q_pos0 + flat % n_q, m, Nc)
     sel = topk(s32, lens, k)
     return s64, s32, sel
