@@ -131,12 +131,12 @@ SplitPlan attn_split_plan(int n_q, long long set_len)
     return {(int)((set_len + len - 1) / len), (int)len};
 }
 
-// lists non-null: the tensor-core decode kernel also collects each row's
-// top-k candidates into them (fused indexer + top-k first pass).
+// wmax non-null: the tensor-core decode kernel also writes each row's warp
+// maxima there (the top-k's collection threshold).
 csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos0, int m, int N_c, int H_I,
                         int d_I, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
                         csa_dtype_t k_dtype, const void* k_scale, float* scores, void* ws, cudaStream_t s,
-                        const TopkLists* lists = nullptr, int k_top = 0)
+                        uint32_t* wmax = nullptr, int wmax_ld = 0)
 {
     if (q_dtype == CSA_F32) {
         return cuda_status(launch_indexer_f32(reinterpret_cast<const float*>(q_idx), q_scale,
@@ -170,13 +170,14 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos
     st = make_map(&tk, keys, dt, (uint64_t)d_I, (uint64_t)B * N_c, (uint64_t)d_I * elem, box_inner, 128);
     if (st != CSA_OK) return st;
     return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, ksc, scores, B, n_q, i_start, n_q_rows, q_pos0, m,
-                                         N_c, num_sms(), lists, k_top, s),
+                                         N_c, num_sms(), wmax, wmax_ld, s),
                        "indexer_tc launch");
 }
 
 // The fused route of csa_index_topk: tensor-core scores of decode groups
 // (fewer than four queries per sequence in the chunk) over rows longer than
-// one top-k CTA's capacity.
+// one top-k CTA's capacity; the indexer also emits the rows' warp maxima, from
+// which the top-k takes its collection threshold.
 bool fused_index_topk(csa_dtype_t q_dtype, int n_q_rows, int N_c, int k)
 {
     return q_dtype != CSA_F32 && indexer_group_tokens(n_q_rows) == 1 && topk_long_rows(N_c, k);
@@ -478,7 +479,8 @@ size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, 
     if (B < 0 || n_q < 0 || N_c < 0 || k < 1) return 0;
     const int rows = index_chunk_rows(B, n_q, N_c);
     return align_up((size_t)B * rows * N_c * 4, 256) + scores_ws_bytes(B, N_c, d_I, k_dtype) +
-           topk_workspace_bytes((long long)B * rows, N_c, k);
+           topk_workspace_bytes((long long)B * rows, N_c, k) +
+           (topk_long_rows(N_c, k) ? topk_wmax_bytes((long long)B * rows, N_c) : 0);
 }
 
 csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
@@ -503,21 +505,19 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
     float* scores = reinterpret_cast<float*>(w);
     uint8_t* w_scores_ws = w + align_up((size_t)B * rows * N_c * 4, 256);
     uint8_t* w_topk = w_scores_ws + scores_ws_bytes(B, N_c, d_I, k_dtype);
+    uint32_t* w_wmax = reinterpret_cast<uint32_t*>(w_topk + topk_workspace_bytes((long long)B * rows, N_c, k));
     for (int i0 = 0; i0 < n_q; i0 += rows) {
         const int nr = std::min(rows, n_q - i0);
         if (N_c > 0 && fused_index_topk(q_dtype, nr, N_c, k)) {
-            // scores and the rows' candidate lists in one kernel, then the
-            // exact select over the lists
-            const long long lrows = (long long)B * nr;
-            const TopkLists lists = topk_lists(w_topk, lrows, k);
-            st = cuda_status(launch_topk_clear_lists(lists, lrows, s), "clear top-k lists");
-            if (st != CSA_OK) return st;
+            // scores plus the rows' warp maxima in one kernel, then the top-k
+            // with its collection threshold taken from them
+            const int ld = topk_wmax_ld(N_c);
             st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                            scores, w_scores_ws, s, &lists, k);
+                            scores, w_scores_ws, s, w_wmax, ld);
             if (st != CSA_OK) return st;
-            st = cuda_status(launch_topk_select_lists(scores, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k,
-                                                      n_q, w_topk, s),
-                             "topk select launch");
+            st = cuda_status(launch_topk(scores, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk,
+                                         s, w_wmax, ld),
+                             "topk launch");
             if (st != CSA_OK) return st;
             continue;
         }

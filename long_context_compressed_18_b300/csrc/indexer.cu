@@ -36,11 +36,7 @@ constexpr int HEADS = 64;         // indexer heads
 constexpr int DIM = 128;          // indexer head dim
 constexpr int ATOM_BYTES_ROW = 128;
 
-// Keys one CTA of the collecting decode kernel covers (its split of a row):
-// their scores stay in shared memory for the candidate selection.
-constexpr int COLLECT_MAX_KEYS = 8192;
-
-template <bool FP8, int T, bool COLLECT = false> struct Cfg {
+template <bool FP8, int T> struct Cfg {
     static constexpr int N = HEADS * T;
     static constexpr int ELEM = FP8 ? 1 : 2;
     static constexpr int ATOMS = DIM * ELEM / ATOM_BYTES_ROW;  // 128-byte K-major column blocks
@@ -51,16 +47,14 @@ template <bool FP8, int T, bool COLLECT = false> struct Cfg {
     static constexpr int Q_BYTES = Q_ATOM * ATOMS;
     static constexpr int K_ATOM = BLOCK_KEYS * ATOM_BYTES_ROW;
     static constexpr int K_BYTES = K_ATOM * ATOMS;
-    static constexpr int STAGES = COLLECT ? 4 : (T == 1) ? 6 : (FP8 ? 6 : 4);
-    static constexpr int SBUF = COLLECT ? COLLECT_MAX_KEYS * 4 : 0;   // the split's scores
+    static constexpr int STAGES = (T == 1) ? 6 : (FP8 ? 6 : 4);
     static constexpr int ACC = (T == 1) ? 4 : 2;
     static constexpr int TMEM_COLS = ACC * N;   // 256 or 512
     static constexpr uint32_t IDESC = instr_desc(FP8 ? 0u : 1u, FP8 ? 0u : 1u, BLOCK_KEYS, N);
     // barriers: full[STAGES], empty[STAGES], acc_full[ACC], acc_empty[ACC], q, mma_done
     static constexpr int N_BARS = 2 * STAGES + 2 * ACC + 2;
     static constexpr int SMEM = 1024 /*align slack*/ + Q_BYTES + STAGES * K_BYTES + N_BARS * 8 +
-                                T * HEADS * 4 + 64 + SBUF;
-    static_assert(!COLLECT || (T == 1 && Q_BYTES >= 2048 * 4), "collection: decode groups; histogram in the Q tile");
+                                T * HEADS * 4 + 64;
 };
 }  // namespace idx
 
@@ -89,124 +83,22 @@ __device__ __forceinline__ float idx_store_score(const uint32_t (&lo)[32], const
     return sc;
 }
 
-// Of the 2048 bins hist[] (counts of one radix level), scanning from the top
-// bin down, the bin where the running count reaches rem (1 <= rem <= total)
-// and the count of all higher bins; NT threads (named barrier 1), et the
-// thread's index among them, scratch NT/32 + 2 shared words.
-template <int NT>
-__device__ __forceinline__ void epi_find_bin(const uint32_t* hist, uint32_t rem, uint32_t* scratch, int et,
-                                             uint32_t& bin, uint32_t& above)
-{
-    constexpr int BPT = 2048 / NT;
-    const int lane = et & 31, w = et >> 5;
-    uint32_t c[BPT], tot = 0;
-#pragma unroll
-    for (int q = 0; q < BPT; ++q) {
-        c[q] = hist[2047 - et * BPT - q];
-        tot += c[q];
-    }
-    uint32_t incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) scratch[w] = incl;
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-    uint32_t before = incl - tot;
-    for (int q = 0; q < w; ++q) before += scratch[q];
-#pragma unroll
-    for (int q = 0; q < BPT; ++q) {
-        if (before < rem && before + c[q] >= rem) {
-            scratch[NT / 32] = (uint32_t)(2047 - et * BPT - q);
-            scratch[NT / 32 + 1] = before;
-        }
-        before += c[q];
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-    bin = scratch[NT / 32];
-    above = scratch[NT / 32 + 1];
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-}
-
-// Candidate collection of one split of a decode row (the epilogue threads of
-// the collecting kernel, after the split's last tile).  The split's n valid
-// scores are in sbuf (entry j0 + e at e).  The threshold c is the key of rank
-// t = 2 k n / L + 32 within the split (twice the split's expected share of the
-// row's top k, plus a margin), rounded down to its 21-bit prefix by two radix
-// levels; every entry with key >= c is appended to the row's list and c is
-// folded into the row's floor (atomicMax), so the select can prove the list
-// complete: the row's k-th largest collected key must be at least every
-// split's c.  t >= n takes the whole split (c = 0).
-template <int NT>
-__device__ void collect_split(const float* sbuf, int n, int j0, int L, int k, uint32_t* hist, uint32_t* scratch,
-                              int et, const TopkLists& lists, long long row)
-{
-    const long long t = 2ll * k * n / L + 32;
-    uint32_t c = 0;
-    if (t < n) {
-        for (int x = et; x < 2048; x += NT) hist[x] = 0;
-        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-        for (int e = et; e < n; e += NT) atomicAdd(&hist[score_key(sbuf[e]) >> 21], 1u);
-        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-        uint32_t b1, above;
-        epi_find_bin<NT>(hist, (uint32_t)t, scratch, et, b1, above);
-        for (int x = et; x < 2048; x += NT) hist[x] = 0;
-        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-        for (int e = et; e < n; e += NT) {
-            const uint32_t key = score_key(sbuf[e]);
-            if ((key >> 21) == b1) atomicAdd(&hist[(key >> 10) & 0x7FFu], 1u);
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-        uint32_t b2, above2;
-        epi_find_bin<NT>(hist, (uint32_t)t - above, scratch, et, b2, above2);
-        c = (b1 << 21) | (b2 << 10);
-    }
-    // count, reserve the split's slice of the row's list, write it
-    uint32_t mine = 0;
-    for (int e = et; e < n; e += NT) mine += score_key(sbuf[e]) >= c;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xFFFFFFFFu, mine, o);
-    if (et == 0) scratch[0] = 0;
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-    if ((et & 31) == 0) atomicAdd(&scratch[0], mine);
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-    if (et == 0) {
-        scratch[1] = atomicAdd(lists.cnt + row, scratch[0]);
-        atomicMax(lists.floor + row, c);
-        scratch[2] = 0;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-    const uint32_t base = scratch[1], cap = (uint32_t)lists.cap;
-    uint32_t* lk = lists.key + row * lists.cap;
-    int32_t* li = lists.idx + row * lists.cap;
-    const unsigned lt = (1u << (et & 31)) - 1u;
-    for (int e0 = 0; e0 < n; e0 += NT) {
-        const int e = e0 + et;
-        const uint32_t key = e < n ? score_key(sbuf[e]) : 0u;
-        const bool take = e < n && key >= c;
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, take);
-        uint32_t p0 = 0;
-        if ((et & 31) == 0 && bal) p0 = atomicAdd(&scratch[2], (uint32_t)__popc(bal));
-        p0 = __shfl_sync(0xFFFFFFFFu, p0, 0);
-        if (take) {
-            const uint32_t pos = base + p0 + __popc(bal & lt);
-            if (pos < cap) {
-                lk[pos] = key;
-                li[pos] = j0 + e;
-            }
-        }
-    }
-}
-
-template <bool FP8, int T, bool COLLECT>
+// WMAX (decode groups, T = 1): for every 32 consecutive keys of a row (one
+// epilogue warp's share of a tile) the largest score key (score_key) is also
+// written to wmax[row * wmax_ld + key / 32].  The k-th largest of a row's warp
+// maxima bounds its k-th largest score from below with at least k entries at
+// or above it, so the top-k needs no sampled threshold.  (Counting the maxima
+// into a per-row histogram with global atomics instead cost the kernel about
+// a quarter of its time: the hot bins serialise.)
+template <bool FP8, int T, bool WMAX>
 __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const float* __restrict__ q_scale, const float* __restrict__ k_scale, float* __restrict__ scores,
     int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int n_splits,
-    int split_tiles, TopkLists lists, int k_top)
+    int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
 {
-    using C = idx::Cfg<FP8, T, COLLECT>;
+    using C = idx::Cfg<FP8, T>;
+    static_assert(!WMAX || T == 1, "warp maxima: decode groups");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base;
@@ -221,7 +113,6 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     float* sq_s = reinterpret_cast<float*>(bars + C::N_BARS);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sq_s + T * idx::HEADS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    float* sbuf = reinterpret_cast<float*>(tmem_holder + 16);   // COLLECT: the split's scores (16-byte aligned)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
@@ -356,24 +247,10 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_acc_empty[acc]);
             const float sc = idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr);
-            if constexpr (COLLECT) sbuf[li * idx::BLOCK_KEYS + row] = sc;
-        }
-        if constexpr (COLLECT) {
-            // every MMA has completed and every copy has landed (the last
-            // accumulator wait), so the query tile is free for the histograms
-            constexpr int NT = 32 * EW;
-            // one read of the abort flag, shared, so that every thread of the
-            // named barriers below takes the same branch
-            volatile uint32_t* go_s = reinterpret_cast<volatile uint32_t*>(sq_s) + 32;
-            asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-            if (et == 0) *go_s = *abort_flag ? 0u : 1u;
-            asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
-            if (*go_s && nv_tok > k_top) {
-                const int n_valid = max(0, min(nv_tok - tile0 * idx::BLOCK_KEYS, n_tiles * idx::BLOCK_KEYS));
-                if (n_valid > 0)
-                    collect_split<NT>(sbuf, n_valid, tile0 * idx::BLOCK_KEYS, nv_tok, k_top,
-                                      reinterpret_cast<uint32_t*>(sQ), reinterpret_cast<uint32_t*>(sq_s), et, lists,
-                                      (long long)b * n_q_rows + i_tok);
+            if constexpr (WMAX) {
+                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, key < nv_tok ? score_key(sc) : 0u);
+                const int grp = (tile0 + li) * (idx::BLOCK_KEYS / 32) + quad;   // keys 32 grp .. 32 grp + 31
+                if (lane == 0 && grp * 32 < nv_tok) wmax[((long long)b * n_q_rows + i_tok) * wmax_ld + grp] = mx;
             }
         }
     }
@@ -485,13 +362,13 @@ cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float
     return cudaGetLastError();
 }
 
-template <bool FP8, int T, bool COLLECT>
+template <bool FP8, int T, bool WMAX>
 static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const float* q_scale,
                              const float* k_scale, float* scores, int B, int n_q_total, int i_start,
-                             int n_q_rows, long long q_pos0, int m, int Nc, int num_sms, const TopkLists& lists,
-                             int k_top, cudaStream_t s)
+                             int n_q_rows, long long q_pos0, int m, int Nc, int num_sms, uint32_t* wmax,
+                             int wmax_ld, cudaStream_t s)
 {
-    using C = idx::Cfg<FP8, T, COLLECT>;
+    using C = idx::Cfg<FP8, T>;
     const int n_groups = (n_q_rows + T - 1) / T;
     long long nv_max = (q_pos0 + i_start + n_q_rows) / m;
     if (nv_max > Nc) nv_max = Nc;
@@ -501,35 +378,32 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     const int per_sm = (C::SMEM <= 113 * 1024) ? 2 : 1;
     const long long target = (long long)num_sms * per_sm * 4;
     int splits = (int)std::min<long long>(tiles, std::max<long long>(1, (target + (long long)B * n_groups - 1) / ((long long)B * n_groups)));
-    // a collecting CTA keeps its split's scores in shared memory
-    if (COLLECT) splits = std::max(splits, (tiles * idx::BLOCK_KEYS + idx::COLLECT_MAX_KEYS - 1) / idx::COLLECT_MAX_KEYS);
     const int split_tiles = (tiles + splits - 1) / splits;
     splits = (tiles + split_tiles - 1) / split_tiles;
-    auto kern = indexer_tc_kernel<FP8, T, COLLECT>;
+    auto kern = indexer_tc_kernel<FP8, T, WMAX>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     dim3 grid(n_groups * splits, B);
     kern<<<grid, idx::threads<T>(), C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, n_q_total, i_start, n_q_rows,
-                                             q_pos0, m, Nc, splits, split_tiles, lists, k_top);
+                                             q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
     return cudaGetLastError();
 }
 
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
                               const float* q_scale, const float* k_scale, float* scores, int B,
                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
-                              int num_sms, const TopkLists* lists, int k_top, cudaStream_t s)
+                              int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s)
 {
-    const TopkLists none{};
-    if (lists) {   // decode groups (T = 1) only
+    if (wmax) {   // decode groups (T = 1) only
         if (T != 1) return cudaErrorInvalidValue;
-        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, *lists, k_top, s);
-        return launch_tc<false, 1, true>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, *lists, k_top, s);
+        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        return launch_tc<false, 1, true>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
     }
     if (fp8) {
-        if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, none, 0, s);
-        return launch_tc<true, 1, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, none, 0, s);
+        if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+        return launch_tc<true, 1, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
     }
-    if (T == 4) return launch_tc<false, 4, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, none, 0, s);
-    return launch_tc<false, 1, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, none, 0, s);
+    if (T == 4) return launch_tc<false, 4, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+    return launch_tc<false, 1, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
 }
 
 int indexer_group_tokens(int n_q) { return n_q >= 4 ? 4 : 1; }

@@ -38,39 +38,27 @@ bool topk_supported(int N_c, int k);
 // rows * chunks of a long row fit one grid dimension (INT_MAX CTAs)
 bool topk_rows_ok(long long rows, int N_c, int k);
 size_t topk_workspace_bytes(long long rows, int N_c, int k);
+// wmax (optional, rows longer than one CTA's capacity): per row, the
+// largest score key of every run of 32 consecutive entries (wmax_ld words a
+// row), written by the decode indexer; the collection then takes its
+// threshold from them instead of from a sample of the row.
 cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
-                        cudaStream_t s);
-// Rows longer than one CTA's capacity are selected from per-row entry lists
-// in the top-k workspace: cnt[r] entries appended (may exceed cap), floor[r]
-// the largest collection threshold any producer of row r used (a list is
-// complete if the k-th largest collected key is at least floor[r]), then cap
-// (key, index) slots per row.  Keys are score_key() of the fp32 scores.
-struct TopkLists {
-    uint32_t* cnt;
-    uint32_t* floor;
-    uint32_t* key;
-    int32_t* idx;
-    int cap;
-};
+                        cudaStream_t s, const uint32_t* wmax = nullptr, int wmax_ld = 0);
 bool topk_long_rows(int N_c, int k);
-TopkLists topk_lists(void* ws, long long rows, int k);
-cudaError_t launch_topk_clear_lists(const TopkLists& w, long long rows, cudaStream_t s);
-// selects every row from its entry list (floors checked), streaming the
-// row's scores where a list is incomplete
-cudaError_t launch_topk_select_lists(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0, int m,
-                                     int N_c, int k, int32_t* out, long long out_b_stride, void* ws, cudaStream_t s);
+int topk_wmax_ld(int N_c);
+size_t topk_wmax_bytes(long long rows, int N_c);
 
 // ---- indexer ----
 int indexer_group_tokens(int n_q);
 int indexer_box_rows(int T);
-// lists non-null (decode groups, T = 1): the epilogue also appends each
-// split's candidates for a top-k of k_top to the rows' entry lists (see
-// TopkLists), which must be cleared first.
+// wmax non-null (decode groups, T = 1): the epilogue also writes, per row
+// (b * n_q_rows + i of the chunk), the largest score key (score_key) of every
+// 32 consecutive visible entries j to wmax[row * wmax_ld + j / 32].
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
                               const float* q_scale, const float* k_scale, float* scores, int B,
                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
-                              int num_sms, const TopkLists* lists, int k_top, cudaStream_t s);
+                              int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s);
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
                                float* scores, int B, int n_q_total, int i_start, int n_q_rows,
                                long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s);

@@ -295,9 +295,14 @@ constexpr int LR_LOCAL_CAP = 4096;   // a chunk's shared-memory list (32 KB: fou
 
 static int lr_cap(int k) { return k * 4 > 8192 ? k * 4 : 8192; }
 
-using LongRowWs = TopkLists;
+struct LongRowWs {
+    uint32_t* cnt;    // [rows] entries collected (may exceed cap); cleared before the collection
+    uint32_t* key;    // [rows][cap]
+    int32_t* idx;     // [rows][cap]
+    int cap;
+};
 
-static size_t lr_head_bytes(long long rows) { return ((size_t)rows * 8 + 255) / 256 * 256; }
+static size_t lr_head_bytes(long long rows) { return ((size_t)rows * 4 + 255) / 256 * 256; }
 
 static LongRowWs lr_ws(void* ws, long long rows, int k)
 {
@@ -305,7 +310,6 @@ static LongRowWs lr_ws(void* ws, long long rows, int k)
     uint8_t* p = reinterpret_cast<uint8_t*>(ws);
     w.cap = lr_cap(k);
     w.cnt = reinterpret_cast<uint32_t*>(p);
-    w.floor = w.cnt + rows;
     p += lr_head_bytes(rows);
     w.key = reinterpret_cast<uint32_t*>(p);
     p += (size_t)rows * w.cap * 4;
@@ -541,9 +545,32 @@ __device__ void collect_entries(const float* __restrict__ row, int c0, int len, 
     }
 }
 
+// Collection threshold from the row's warp maxima (wmax: the largest score
+// key of each run of 32 consecutive entries, written by the indexer): the
+// exact kk-th largest of the nw = ceil(L / 32) maxima.  Those kk maxima are
+// distinct entries, so at least kk entries have a key at or above it: every
+// entry of the row's top kk does, and collecting key >= it is complete.  With
+// fewer maxima than kk, 0 (take every entry).  keys: shared buffer of nw keys.
+__device__ uint32_t wmax_threshold(const uint32_t* __restrict__ wrow, int nw, int kk, uint32_t* keys, TopkShared& sh)
+{
+    if (nw < kk) return 0u;
+    clear_hist(sh, 2048);
+    __syncthreads();
+    for (int x = threadIdx.x; x < nw; x += TOPK_THREADS) {
+        const uint32_t key = __ldcg(wrow + x);
+        keys[x] = key;
+        atomicAdd(&sh.hist[key >> 21], 1u);
+    }
+    __syncthreads();
+    uint32_t T;
+    int teq;
+    radix_threshold(keys, nw, kk, sh, T, teq);
+    return T;
+}
+
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    int n_chunks, LongRowWs w)
+    int n_chunks, LongRowWs w, const uint32_t* __restrict__ wmax, int wmax_ld)
 {
     // the chunk's entries go to a shared-memory list, then one global atomic
     // reserves the chunk's slice of the row's list (whose order does not
@@ -558,10 +585,15 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
     if (L <= k) return;
     const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
     if (len == 0) return;
-    // every chunk CTA of the row derives the same threshold from the same
-    // samples (the list's storage holds the sample keys meanwhile)
+    // every chunk CTA of the row derives the same threshold, from the row's
+    // warp maxima when the indexer wrote them (and they fit the chunk list's
+    // storage, which holds them meanwhile), else from the same samples
     static_assert(LR_LOCAL_CAP >= LR_SAMPLES, "sample keys live in the chunk list");
-    const uint32_t thr = sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, lkey, sh);
+    const int nw = (L + 31) / 32;
+    const uint32_t thr = (wmax && nw <= 2 * LR_LOCAL_CAP)
+                             ? wmax_threshold(wmax + (long long)r * wmax_ld, nw, min(k, L), lkey, sh)
+                             : sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, lkey, sh);
+    __syncthreads();
     if (threadIdx.x == 0) n_loc_s = 0;
     __syncthreads();
     const uint32_t cap = (uint32_t)w.cap;
@@ -594,15 +626,8 @@ __host__ __device__ constexpr int bitmap_words(int L) { return (((L + 31) / 32) 
 // n >= kk) -- the top kk by (score desc, index asc) -- written to o in
 // ascending index order.  bitmaps: shared memory for two bitmaps of
 // bitmap_words(L) words each (16-byte aligned).
-//
-// need: the largest threshold any producer of the list collected at (0 when
-// the list holds every entry at or above one threshold).  The list is then
-// complete only if the k-th largest key among its entries is at least need
-// (every entry of the row at or above that key was collected); otherwise
-// nothing is written and false is returned, for the caller to select by
-// streaming the row.
-__device__ bool select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* bitmaps,
-                               TopkShared& sh, int32_t* __restrict__ o, uint32_t need = 0u)
+__device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* bitmaps,
+                               TopkShared& sh, int32_t* __restrict__ o)
 {
     const int tid = threadIdx.x;
     const int nw = (L + 31) / 32, nw4 = bitmap_words(L);
@@ -648,8 +673,6 @@ __device__ bool select_entries(uint32_t* ekey, const int32_t* eidx, int n, int k
     int teq;
     radix_threshold(ekey, n, kk, sh, T, teq, &n_eq);
     __syncthreads();
-    // T is the spread key of a collected entry: its key is lo + (T >> shl)
-    if (lo + (T >> shl) < need) return false;   // uniform: every thread holds the same T
     // mark the selection; keys equal to T join it directly unless only some
     // of them are taken (then the first teq in index order, below)
     const bool all_eq = n_eq == (uint32_t)teq;
@@ -748,7 +771,6 @@ __device__ bool select_entries(uint32_t* ekey, const int32_t* eidx, int n, int k
             if (pos < (uint32_t)kk) o[pos] = j;
         }
     }
-    return true;
 }
 
 // Exact selection of a row's top kk streamed from global memory: the three
@@ -789,7 +811,7 @@ __device__ void select_streaming(const float* __restrict__ row, int L, int kk, T
 
 __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
-    LongRowWs w, int fast_ok, int use_floor, int32_t* __restrict__ out, long long out_b_stride)
+    LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
@@ -831,9 +853,8 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
             }
         }
         __syncthreads();
-        const uint32_t need = use_floor ? __ldcg(w.floor + r) : 0u;
-        if (select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o, need)) return;
-        __syncthreads();
+        select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o);
+        return;
     }
     select_streaming(row, L, kk, sh, o);
 }
@@ -929,21 +950,21 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k)
 // bitmaps of the row and the entry list in shared memory; shapes beyond that
 // stream every row instead.
 static cudaError_t launch_select(const float* scores, long long ld, int n_q_rows, long long q_pos0, int m, int N_c,
-                                 int k, const LongRowWs& w, int rows, int use_floor, int32_t* out,
-                                 long long out_b_stride, cudaStream_t s)
+                                 int k, const LongRowWs& w, int rows, int32_t* out, long long out_b_stride,
+                                 cudaStream_t s)
 {
     size_t smem = (size_t)2 * bitmap_words(N_c) * 4 + (size_t)w.cap * 8;
     const int fast_ok = smem <= (size_t)200 * 1024;
     if (!fast_ok) smem = 0;
     cudaFuncSetAttribute(topk_lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    topk_lr_select_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok,
-                                                          use_floor, out, out_b_stride);
+    topk_lr_select_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok, out,
+                                                          out_b_stride);
     return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
-                        cudaStream_t s)
+                        cudaStream_t s, const uint32_t* wmax, int wmax_ld)
 {
     const long long rows_ll = (long long)B * n_q_rows;
     if (rows_ll == 0) return cudaSuccess;
@@ -964,33 +985,22 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
-    cudaError_t e = launch_topk_clear_lists(w, rows, s);
+    cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)rows * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
     cudaFuncSetAttribute(topk_lr_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     topk_lr_collect_kernel<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
-                                                                          p.n_chunks, w);
-    return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, rows, 0, out, out_b_stride, s);
+                                                                          p.n_chunks, w, wmax, wmax_ld);
+    return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, rows, out, out_b_stride, s);
 }
-
-TopkLists topk_lists(void* ws, long long rows, int k) { return lr_ws(ws, rows, k); }
 
 bool topk_long_rows(int N_c, int k) { return topk_plan(N_c, k).n_chunks > 1; }
 
-cudaError_t launch_topk_clear_lists(const TopkLists& w, long long rows, cudaStream_t s)
-{
-    // the counters and the collection floors (adjacent)
-    return cudaMemsetAsync(w.cnt, 0, (size_t)rows * 2 * sizeof(uint32_t), s);
-}
+int topk_wmax_ld(int N_c) { return (N_c + 31) / 32; }
 
-cudaError_t launch_topk_select_lists(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0, int m,
-                                     int N_c, int k, int32_t* out, long long out_b_stride, void* ws, cudaStream_t s)
+size_t topk_wmax_bytes(long long rows, int N_c)
 {
-    const long long rows = (long long)B * n_q_rows;
-    if (rows == 0) return cudaSuccess;
-    if (!topk_rows_ok(rows, N_c, k)) return cudaErrorInvalidConfiguration;
-    return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, lr_ws(ws, rows, k), (int)rows, 1, out,
-                         out_b_stride, s);
+    return ((size_t)rows * topk_wmax_ld(N_c) * 4 + 255) / 256 * 256;
 }
 
 }  // namespace csa

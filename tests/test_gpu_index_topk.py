@@ -1,11 +1,12 @@
 """GPU parity of csa_index_topk's fused route: for decode-shaped calls over
-rows longer than one top-k CTA, the indexer kernel keeps each key split's
-scores on chip and appends that split's candidates to the row's list, and the
-select kernel proves the list complete (or streams the row).  The result must
-be bit-identical to scoring and selecting in two calls -- both routes are
-exact -- and agree with the oracle up to near-ties, including on rows built
-so that the lists are incomplete (the best entries clustered in one split) or
-overflow (every score equal)."""
+rows longer than one top-k CTA, the indexer kernel also writes each row's
+warp maxima (the largest score of every 32 consecutive entries), and the
+top-k takes its collection threshold from them -- the k-th largest warp
+maximum, below which at least k entries lie -- instead of sampling the row.
+The result must be bit-identical to scoring and selecting in two calls (both
+routes are exact) and agree with the oracle up to near-ties, including on rows
+built so that the collection overflows and the select streams the row (the
+best entries clustered at the end of the row, or every score equal)."""
 import numpy as np
 import pytest
 import torch
@@ -88,7 +89,7 @@ def test_fused_short_and_long_rows_in_one_call():
     """Queries early in the context see at most k entries (no selection), later
     ones more; the split CTAs of short rows collect nothing."""
     B, n_q, Nc, k = 2, 3, 50000, 1024
-    q_pos0 = 4 * 1024 + 2          # rows of 1024, 1024 and 1025 visible entries
+    q_pos0 = 4 * 1024 + 1          # rows of 1024, 1024 and 1025 visible entries
     q, qd, qs, kk, kd, ks = _inputs(B, n_q, Nc, "e4m3", seed=5)
     args = (B, n_q, q_pos0, 4, Nc, k, _dev(q), qd, _dev(qs), _dev(kk), kd, _dev(ks))
     got = _fused(*args)
@@ -110,12 +111,11 @@ def _structured_keys(B, Nc, scale_of_j):
 
 
 @pytest.mark.parametrize("shape", ["ascending", "equal"])
-def test_fused_incomplete_lists_fall_back_exactly(shape):
-    """ascending: the row's best entries all sit in its last split, which
-    collects only about twice its expected share, so the collected k-th key
-    lies below that split's threshold and the select must stream the row.
-    equal: every score ties, every split takes its whole range, the list
-    overflows, and the first k indices win."""
+def test_fused_overflowing_collection_falls_back_exactly(shape):
+    """ascending: the k best warp maxima are the last k runs of 32 entries, so
+    the threshold takes all 32k of their entries, more than the row's list
+    holds, and the select streams the row.  equal: every score ties, every
+    entry is collected, and the first k indices win."""
     B, Nc, k = 2, 262144, 1024
     fn = (lambda j: 1.0 + j * 2.0 ** -18) if shape == "ascending" else (lambda j: torch.ones_like(j))
     q, qd, qs, kk, kd, ks = _structured_keys(B, Nc, fn)
