@@ -253,6 +253,8 @@ static csa_status_t run_attn_tc(int mode, int B, int n_q, int64_t q_pos0, int m,
     if (st != CSA_OK) return st;
     AttnTcParams p{};
     p.topk = topk;
+    p.k_rows = reinterpret_cast<const __nv_bfloat16*>(kp);
+    p.v_rows = reinterpret_cast<const __nv_bfloat16*>(vp);
     p.out = reinterpret_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     p.q_pos0 = q_pos0;

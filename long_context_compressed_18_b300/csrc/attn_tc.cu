@@ -20,14 +20,10 @@
 // token x H heads (sparse mode: every token has its own key set; with H = 64
 // the upper 64 rows idle).
 //
-// Warp roles (224 threads):
-//   warps 0-1  producers: Q once, then K and V tiles into rings of STAGES
-//              buffers (a K stage is released when S_j completes, a V stage
-//              when P_j V_j completes) -- tiled TMA for the dense modes; for
-//              the sparse mode TMA tile::gather4 row gathers (4 selected rows
-//              of 64 columns per instruction) issued by all 64 lanes of both
-//              warps: one warp's issue rate tops out near 7 bytes per cycle
-//              per SM, two reach the latency limit of the ring;
+// Warp roles.  Dense modes (224 threads):
+//   warps 0-1  producer: Q once, then K and V tiles into rings of STAGES
+//              buffers by tiled TMA (a K stage is released when S_j
+//              completes, a V stage when P_j V_j completes);
 //   warp 2     TMEM owner and single-thread MMA issuer: S_j into one of two S
 //              buffers, then O += P_{j-1} V_{j-1}, so the QK^T of tile j
 //              overlaps the softmax of tile j-1;
@@ -35,6 +31,18 @@
 //              the base-2 domain against a lazily moved reference maximum,
 //              P written back to TMEM as bf16; O and l are rescaled (in TMEM)
 //              only when a row's maximum grows by more than 2^8.
+// Sparse mode (512 threads): the selected rows are scattered, and fetching
+// them sets the pace, so eight warps gather them with 16-byte cp.async
+// (about 1.8x the rate of TMA tile::gather4 from two warps on an L2-resident
+// table: 23.7 vs 12.9 bytes per cycle per SM, measured on B300); each gather
+// warp publishes tile j after issuing tile j+1, once its own copies of tile j
+// have landed (cp.async.wait_group, then a proxy fence, then its arrival).
+//   warps 0-3  softmax and epilogue, two passes over 32-column chunks of S
+//              (row maximum, then exponentials) so that they fit the 128
+//              registers a thread of a 512-thread CTA has;
+//   warp 4     TMEM owner and MMA issuer, as above;
+//   warps 8-15 gather warps: Q by TMA once, the CTA's selection list into
+//              shared memory, then the K and V rows of every tile.
 // Every mbarrier wait is bounded; on a timeout the CTA drains its copies and
 // MMAs, frees TMEM and exits with the device status word set.
 //
@@ -47,7 +55,17 @@
 namespace csa {
 
 namespace atc {
-constexpr int THREADS = 224;
+// warp roles per mode (see the header)
+template <int MODE> struct Roles {
+    static constexpr bool SPARSE = MODE == 0;
+    static constexpr int THREADS = SPARSE ? 512 : 224;
+    static constexpr int MMA_WARP = SPARSE ? 4 : 2;
+    static constexpr int SOFTMAX_WARP0 = SPARSE ? 0 : 3;   // four consecutive warps
+    static constexpr int GATHER_WARP0 = 8;                  // sparse mode: eight gather warps
+    static constexpr int GATHER_WARPS = 8;
+};
+static_assert(Roles<0>::GATHER_WARP0 + Roles<0>::GATHER_WARPS <= Roles<0>::THREADS / 32 &&
+                  Roles<0>::GATHER_WARP0 > Roles<0>::MMA_WARP, "gather warps inside the CTA, after the others");
 constexpr int ROWS = 128;                 // MMA M
 constexpr int KT = 128;                   // keys per tile
 constexpr int D = 128;                    // head dim
@@ -77,12 +95,13 @@ template <int MODE, int STAGES, int QROWS> struct Cfg {
 }  // namespace atc
 
 template <int MODE, int STAGES, int QROWS>
-__global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
+__global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v, const AttnTcParams p)
 {
     using namespace atc;
     using C = Cfg<MODE, STAGES, QROWS>;
+    using R = Roles<MODE>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base;
@@ -134,8 +153,9 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
         mbar_init(bar_mma_done, 1);
         mbar_init(bar_list, 1);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
+            // sparse mode: one arrival per gather warp; dense: the TMA issuer
+            mbar_init(&k_full[s], R::SPARSE ? R::GATHER_WARPS : 1);
+            mbar_init(&v_full[s], R::SPARSE ? R::GATHER_WARPS : 1);
             mbar_init(&k_empty[s], 1);
             mbar_init(&v_empty[s], 1);
         }
@@ -147,7 +167,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 2) {
+    if (warp == R::MMA_WARP) {
         tmem_alloc(tmem_holder, TMEM_COLS);
         tmem_relinquish();
     }
@@ -156,48 +176,101 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp < 2) {
-        // ------------------------------ producers ------------------------------
-        const int pl = warp * 32 + lane;                     // 0..63
-        if (n_tiles > 0 && (MODE == 0 || warp == 0)) {
-            if (pl == 0) {
+    if (R::SPARSE && warp >= R::GATHER_WARP0 && warp < R::GATHER_WARP0 + R::GATHER_WARPS) {
+        // ------------------------- gather warps (sparse) -------------------------
+        constexpr int GT = 32 * R::GATHER_WARPS;             // gather threads
+        const int gl = (warp - R::GATHER_WARP0) * 32 + lane;  // 0 .. GT-1
+        if (n_tiles > 0) {
+            if (gl == 0) {
                 tma_prefetch_desc(&tmap_q);
-                if (MODE != 0) {
-                    tma_prefetch_desc(&tmap_k);
-                    tma_prefetch_desc(&tmap_v);
-                }
                 const int qrow = (b * p.n_q + i0) * p.H;
                 mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
                 tma_load_2d(sQ, &tmap_q, bar_q, 0, qrow);
                 tma_load_2d(sQ + C::Q_ATOM, &tmap_q, bar_q, 64, qrow);
             }
-            if constexpr (MODE == 0) {
-                // stage the CTA's slice of the selection list once (invalid -> -1),
-                // padded with -1 to whole tiles; eight loads in flight per lane
-                const int32_t* sel = p.topk + ((long long)b * p.n_q + i0) * p.k;
-                const int len = (int)(r_hi - r_lo), padded = n_tiles * KT;
-                for (int base0 = 0; base0 < padded; base0 += 64 * 8) {
-                    int v[8];
+            // stage the CTA's slice of the selection list once (invalid -> -1),
+            // padded with -1 to whole tiles
+            const int32_t* sel = p.topk + ((long long)b * p.n_q + i0) * p.k;
+            const int len = (int)(r_hi - r_lo), padded = n_tiles * KT;
+            for (int base0 = 0; base0 < padded; base0 += GT * 4) {
+                int v[4];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int e = base0 + u * 64 + pl;
-                        v[u] = e < len ? __ldg(sel + r_lo + e) : -1;
-                    }
+                for (int u = 0; u < 4; ++u) {
+                    const int e = base0 + u * GT + gl;
+                    v[u] = e < len ? __ldg(sel + r_lo + e) : -1;
+                }
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int e = base0 + u * 64 + pl;
-                        if (e < padded) {
-                            int idx = v[u];
-                            if (idx >= p.N_kv || idx < -1) {
-                                flag_status(STATUS_BOUNDS);
-                                idx = -1;
-                            }
-                            sidx[e] = idx;
+                for (int u = 0; u < 4; ++u) {
+                    const int e = base0 + u * GT + gl;
+                    if (e < padded) {
+                        int idx = v[u];
+                        if (idx >= p.N_kv || idx < -1) {
+                            flag_status(STATUS_BOUNDS);
+                            idx = -1;
                         }
+                        sidx[e] = idx;
                     }
                 }
-                asm volatile("bar.sync 1, 64;" ::: "memory");
-                if (pl == 0) mbar_arrive(bar_list);
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(GT) : "memory");
+            if (gl == 0) mbar_arrive(bar_list);
+            // K and V rows of tile j: 128 rows x 16 chunks of 16 bytes each,
+            // written into the 128-byte-swizzled K-major layout (the chunk
+            // index within a 128-byte row XORed with the row's low 3 bits);
+            // invalid entries fetch row 0 (the softmax masks them)
+            const long long bN = (long long)b * p.N_kv;
+            auto gather = [&](const __nv_bfloat16* __restrict__ src, uint8_t* dst, int j) {
+#pragma unroll
+                for (int c0 = 0; c0 < KT * 16; c0 += GT) {
+                    const int c = c0 + gl;
+                    const int r = c >> 4, ch = c & 15;
+                    const long long row = bN + max(sidx[j * KT + r], 0);
+                    cp_async16(dst + (ch >> 3) * ATOM + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                               src + row * D + ch * 8);
+                }
+                cp_async_commit();
+            };
+            auto publish = [&](int j) {
+                // this warp's copies of tile j have landed: make them visible
+                // to the tensor cores, then arrive
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&k_full[j % STAGES]);
+                    mbar_arrive(&v_full[j % STAGES]);
+                }
+            };
+            bool ok = true;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % STAGES;
+                const uint32_t par = ((j / STAGES) & 1) ^ 1;
+                int w = 1;
+                if (lane == 0) w = mbar_wait(&k_empty[st], par, abort_flag);
+                if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
+                gather(p.k_rows, sK + st * K_BYTES, j);
+                if (lane == 0) w = mbar_wait(&v_empty[st], par, abort_flag);
+                if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
+                gather(p.v_rows, sV + st * V_BYTES, j);
+                if (j >= 1) {
+                    cp_async_wait<2>();        // tile j-1's two groups have landed
+                    publish(j - 1);
+                }
+            }
+            cp_async_wait<0>();                // nothing of this warp is left in flight
+            if (ok) publish(n_tiles - 1);
+            if (gl == 0 && *abort_flag) mbar_wait(bar_q, 0);   // the Q copy lands before the CTA exits
+        }
+    } else if (!R::SPARSE && warp < 2) {
+        // ------------------------ producer (dense modes) ------------------------
+        if (n_tiles > 0 && warp == 0) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tmap_q);
+                tma_prefetch_desc(&tmap_k);
+                tma_prefetch_desc(&tmap_v);
+                const int qrow = (b * p.n_q + i0) * p.H;
+                mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
+                tma_load_2d(sQ, &tmap_q, bar_q, 0, qrow);
+                tma_load_2d(sQ + C::Q_ATOM, &tmap_q, bar_q, 64, qrow);
             }
             int issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
@@ -206,39 +279,22 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                 int ok = 1;
                 if (lane == 0) ok = mbar_wait(&k_empty[st], par, abort_flag);
                 if (!__shfl_sync(FULL, ok, 0)) break;
-                if constexpr (MODE == 0) {
-                    // 32 groups of 4 rows x 2 column blocks per tile: lane l of
-                    // warp w gathers rows 4l..4l+3, columns 64w..64w+63 (invalid
-                    // entries fetch row 0; the softmax masks them)
-                    const int4 q4 = reinterpret_cast<const int4*>(sidx + j * KT)[lane];
-                    const int bN = b * p.N_kv;
-                    const int r0 = bN + max(q4.x, 0), r1 = bN + max(q4.y, 0);
-                    const int r2 = bN + max(q4.z, 0), r3 = bN + max(q4.w, 0);
-                    const uint32_t off = (uint32_t)(warp * ATOM + lane * 512);
-                    if (pl == 0) mbar_arrive_expect_tx(&k_full[st], K_BYTES);
-                    tma_gather4(sK + st * K_BYTES + off, &tmap_k, &k_full[st], warp * 64, r0, r1, r2, r3);
-                    if (lane == 0) ok = mbar_wait(&v_empty[st], par, abort_flag);
-                    if (!__shfl_sync(FULL, ok, 0)) break;
-                    if (pl == 0) mbar_arrive_expect_tx(&v_full[st], V_BYTES);
-                    tma_gather4(sV + st * V_BYTES + off, &tmap_v, &v_full[st], warp * 64, r0, r1, r2, r3);
-                } else {
-                    const int krow = (int)((long long)b * p.N_kv + r_lo + (long long)j * KT);
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&k_full[st], K_BYTES);
-                        tma_load_2d(sK + st * K_BYTES, &tmap_k, &k_full[st], 0, krow);
-                        tma_load_2d(sK + st * K_BYTES + ATOM, &tmap_k, &k_full[st], 64, krow);
-                        ok = mbar_wait(&v_empty[st], par, abort_flag);
-                    }
-                    if (!__shfl_sync(FULL, ok, 0)) break;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&v_full[st], V_BYTES);
-                        tma_load_2d(sV + st * V_BYTES, &tmap_v, &v_full[st], 0, krow);
-                        tma_load_2d(sV + st * V_BYTES + ATOM, &tmap_v, &v_full[st], 64, krow);
-                    }
+                const int krow = (int)((long long)b * p.N_kv + r_lo + (long long)j * KT);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&k_full[st], K_BYTES);
+                    tma_load_2d(sK + st * K_BYTES, &tmap_k, &k_full[st], 0, krow);
+                    tma_load_2d(sK + st * K_BYTES + ATOM, &tmap_k, &k_full[st], 64, krow);
+                    ok = mbar_wait(&v_empty[st], par, abort_flag);
+                }
+                if (!__shfl_sync(FULL, ok, 0)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&v_full[st], V_BYTES);
+                    tma_load_2d(sV + st * V_BYTES, &tmap_v, &v_full[st], 0, krow);
+                    tma_load_2d(sV + st * V_BYTES + ATOM, &tmap_v, &v_full[st], 64, krow);
                 }
                 issued = j + 1;
             }
-            if (pl == 0 && *abort_flag) {
+            if (lane == 0 && *abort_flag) {
                 // let the copies already in flight land before the CTA exits
                 mbar_wait(bar_q, 0);
                 for (int j = max(0, issued - STAGES); j < issued; ++j) {
@@ -247,7 +303,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                 }
             }
         }
-    } else if (warp == 2) {
+    } else if (warp == R::MMA_WARP) {
         // --------------------------- MMA issuer ---------------------------
         if (lane == 0 && n_tiles > 0) {
             const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
@@ -292,7 +348,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
             umma_commit(bar_mma_done);      // all MMAs of this CTA retired
             mbar_wait(bar_mma_done, 0);
         }
-    } else {
+    } else if (warp >= R::SOFTMAX_WARP0 && warp < R::SOFTMAX_WARP0 + 4) {
         // ----------------------- softmax + epilogue -----------------------
         // Online softmax in the base-2 domain with a lazily moved reference
         // maximum m_ref: P_j = 2^(s * scale * log2 e - m_ref) is accumulated
@@ -353,69 +409,115 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
                     hi_c = (int)(e < 0 ? 0 : (e > KT ? KT : e));
                 }
                 const uint32_t s_addr = tmem + lane_base + S_COL + sb * KT;
-                float sv[KT];
-#pragma unroll
-                for (int q = 0; q < KT / 32; ++q) tmem_ld32(s_addr + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
-                tmem_ld_wait();
-                // masked columns become -inf; a tile valid for every row of the
-                // warp (the common case) skips the masking
-                const bool full_row = (MODE == 0) ? (row_ok && (mk[0] & mk[1] & mk[2] & mk[3]) == FULL)
-                                                  : (lo_c == 0 && hi_c == KT);
-                if (!__all_sync(FULL, full_row)) {
-#pragma unroll
-                    for (int c = 0; c < KT; ++c) {
-                        const bool v = (MODE == 0) ? ((mk[c & 3] >> (c >> 2)) & 1u)
-                                                   : ((unsigned)(c - lo_c) < (unsigned)(hi_c - lo_c));
-                        sv[c] = v ? sv[c] : -INFINITY;
-                    }
-                }
-                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < KT; c += 8) {
-                    a0 = fmax3(a0, sv[c], sv[c + 1]);
-                    a1 = fmax3(a1, sv[c + 2], sv[c + 3]);
-                    a2 = fmax3(a2, sv[c + 4], sv[c + 5]);
-                    a3 = fmax3(a3, sv[c + 6], sv[c + 7]);
-                }
-                // scores are raw dot products; the positive scale commutes with max
-                const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2;
-                // move the reference maximum if this tile exceeds it by > 2^8
-                const bool move = mx > m_ref + RESCALE_LOG2;
-                const float m_new = move ? mx : m_ref;
-                if (__any_sync(FULL, move && m_ref != -INFINITY)) {
-                    // O holds P_0..P_{j-1} V against the old reference: wait
-                    // for P_{j-1} V_{j-1}, then rescale the rows that moved
-                    const bool w2 = mbar_wait(o_full, (j - 1) & 1, abort_flag);
-                    if (!__all_sync(FULL, w2)) { ok = false; break; }
-                    tc_fence_after();
-                    const float f = (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
-                    const uint32_t o_addr = tmem + lane_base + O_COL;
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        uint32_t ov[32];
-                        tmem_ld32(o_addr + 32 * q, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
-                        tmem_st32(o_addr + 32 * q, ov);
-                    }
-                    l_run *= f;
-                }
-                m_ref = m_new;
-                const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 float sum = 0.f;
+                // the rescale of O when this tile's maximum moves the reference;
+                // false on a timeout
+                auto move_reference = [&](float mx) -> bool {
+                    const bool move = mx > m_ref + RESCALE_LOG2;
+                    const float m_new = move ? mx : m_ref;
+                    if (__any_sync(FULL, move && m_ref != -INFINITY)) {
+                        // O holds P_0..P_{j-1} V against the old reference: wait
+                        // for P_{j-1} V_{j-1}, then rescale the rows that moved
+                        const bool w2 = mbar_wait(o_full, (j - 1) & 1, abort_flag);
+                        if (!__all_sync(FULL, w2)) return false;
+                        tc_fence_after();
+                        const float f = (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
+                        const uint32_t o_addr = tmem + lane_base + O_COL;
 #pragma unroll
-                for (int q = 0; q < KT / 32; ++q) {
-                    uint32_t pk[16];
+                        for (int q = 0; q < D / 32; ++q) {
+                            uint32_t ov[32];
+                            tmem_ld32(o_addr + 32 * q, ov);
+                            tmem_ld_wait();
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const float p0 = ex2_approx(fmaf(sv[32 * q + 2 * u], sl2, neg_m));
-                        const float p1 = ex2_approx(fmaf(sv[32 * q + 2 * u + 1], sl2, neg_m));
-                        sum += p0 + p1;
-                        pk[u] = pack_bf16x2(p0, p1);
+                            for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
+                            tmem_st32(o_addr + 32 * q, ov);
+                        }
+                        l_run *= f;
                     }
-                    // P columns 16q..16q+15 overwrite S columns already read
-                    tmem_st16(s_addr + 16 * q, pk);
+                    m_ref = m_new;
+                    return true;
+                };
+                if constexpr (R::SPARSE) {
+                    // two passes over 32-column chunks of S: the row maximum,
+                    // then the exponentials (a chunk's P overwrites S columns
+                    // already read: P of chunk q lands in columns 16q .. 16q+15)
+                    const bool all_full = __all_sync(FULL, row_ok && (mk[0] & mk[1] & mk[2] & mk[3]) == FULL);
+                    auto load_chunk = [&](int q, float (&v)[32]) {
+                        tmem_ld32(s_addr + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                        tmem_ld_wait();
+                        if (!all_full) {
+#pragma unroll
+                            for (int u = 0; u < 32; ++u) {
+                                const int c = 32 * q + u;
+                                v[u] = ((mk[c & 3] >> (c >> 2)) & 1u) ? v[u] : -INFINITY;
+                            }
+                        }
+                    };
+                    float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+                    for (int q = 0; q < KT / 32; ++q) {
+                        float v[32];
+                        load_chunk(q, v);
+#pragma unroll
+                        for (int u = 0; u < 32; u += 4) {
+                            a0 = fmax3(a0, v[u], v[u + 1]);
+                            a1 = fmax3(a1, v[u + 2], v[u + 3]);
+                        }
+                    }
+                    // scores are raw dot products; the positive scale commutes with max
+                    if (!move_reference(fmaxf(a0, a1) * sl2)) { ok = false; break; }
+                    const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+#pragma unroll
+                    for (int q = 0; q < KT / 32; ++q) {
+                        float v[32];
+                        load_chunk(q, v);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const float p0 = ex2_approx(fmaf(v[2 * u], sl2, neg_m));
+                            const float p1 = ex2_approx(fmaf(v[2 * u + 1], sl2, neg_m));
+                            sum += p0 + p1;
+                            pk[u] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(s_addr + 16 * q, pk);
+                    }
+                } else {
+                    float sv[KT];
+#pragma unroll
+                    for (int q = 0; q < KT / 32; ++q) tmem_ld32(s_addr + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q]));
+                    tmem_ld_wait();
+                    // masked columns become -inf; a tile valid for every row of the
+                    // warp (the common case) skips the masking
+                    const bool full_row = lo_c == 0 && hi_c == KT;
+                    if (!__all_sync(FULL, full_row)) {
+#pragma unroll
+                        for (int c = 0; c < KT; ++c)
+                            sv[c] = ((unsigned)(c - lo_c) < (unsigned)(hi_c - lo_c)) ? sv[c] : -INFINITY;
+                    }
+                    float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < KT; c += 8) {
+                        a0 = fmax3(a0, sv[c], sv[c + 1]);
+                        a1 = fmax3(a1, sv[c + 2], sv[c + 3]);
+                        a2 = fmax3(a2, sv[c + 4], sv[c + 5]);
+                        a3 = fmax3(a3, sv[c + 6], sv[c + 7]);
+                    }
+                    // scores are raw dot products; the positive scale commutes with max
+                    if (!move_reference(fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * sl2)) { ok = false; break; }
+                    const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+#pragma unroll
+                    for (int q = 0; q < KT / 32; ++q) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const float p0 = ex2_approx(fmaf(sv[32 * q + 2 * u], sl2, neg_m));
+                            const float p1 = ex2_approx(fmaf(sv[32 * q + 2 * u + 1], sl2, neg_m));
+                            sum += p0 + p1;
+                            pk[u] = pack_bf16x2(p0, p1);
+                        }
+                        // P columns 16q..16q+15 overwrite S columns already read
+                        tmem_st16(s_addr + 16 * q, pk);
+                    }
                 }
                 tmem_st_wait();
                 l_run += sum;
@@ -482,7 +584,7 @@ __global__ void __launch_bounds__(atc::THREADS, 1) attn_tc_kernel(
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == R::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -501,7 +603,7 @@ static void launch_one(dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk, 
     auto kern = attn_tc_kernel<MODE, STAGES, QROWS>;
     constexpr int smem = atc::Cfg<MODE, STAGES, QROWS>::SMEM;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    kern<<<grid, atc::THREADS, smem, s>>>(tq, tk, tv, p);
+    kern<<<grid, atc::Roles<MODE>::THREADS, smem, s>>>(tq, tk, tv, p);
 }
 
 cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

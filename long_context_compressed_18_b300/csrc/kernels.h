@@ -92,6 +92,8 @@ cudaError_t launch_attn_combine(const AttnArgsT<__nv_bfloat16>& a, int H, int D,
 // 64-column boxes with 128-byte swizzle.
 struct AttnTcParams {
     const int32_t* topk;   // [B, n_q, k] (mode 0)
+    const __nv_bfloat16* k_rows;   // K [B * N_kv, 128] (mode 0: rows gathered with cp.async)
+    const __nv_bfloat16* v_rows;   // V [B * N_kv, 128]
     __nv_bfloat16* out;    // [B, n_q, H, 128]
     float* lse;            // [B, n_q, H] or null
     float* part_o;         // [n_splits, B*n_q, H, 128] when n_splits > 1
