@@ -41,6 +41,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=0, help="override the decode batch (profiling runs)")
+    p.add_argument("--scores", default="f32", choices=["f32", "bf16"],
+                   help="index-score storage of the decode step (bf16: the pages' BF16 score variant)")
     return p.parse_args()
 
 
@@ -192,7 +194,8 @@ def run_decode(args, torch, dist, rank, world):
     topk = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
     out = torch.empty(B, 1, H, d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, 1, H, dtype=torch.float32, device="cuda")
-    ws_t_b = lib.csa_index_topk_workspace_size(B, 1, Nc, HI, dI, k, lib.E4M3)
+    sdt = lib.BF16 if args.scores == "bf16" else lib.F32
+    ws_t_b = lib.csa_index_topk_workspace_size(B, 1, Nc, HI, dI, k, lib.E4M3, sdt)
     ws_a_b = lib.csa_sparse_attn_workspace_size(B, 1, H, d, k)
     ws_t = lib.empty_workspace(ws_t_b)
     ws_a = lib.empty_workspace(ws_a_b)
@@ -206,7 +209,7 @@ def run_decode(args, torch, dist, rank, world):
         if ev:
             ev[0].record(stream)
         lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, x["idx_q"], lib.E4M3, x["idx_q_scale"],
-                           x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], topk, ws_t, ws_t_b)
+                           x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], topk, ws_t, ws_t_b, score_dtype=sdt)
         if ev:
             ev[1].record(stream)
         lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, x["q"], x["k_c"], x["v_c"], lib.BF16, topk, out, lse,
@@ -314,7 +317,7 @@ def run_decode(args, torch, dist, rank, world):
             if used[j]:
                 stream.wait_event(down_done[j])           # step i-2's results have left these buffers
             lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, di["idx_q"], lib.E4M3, di["idx_q_scale"],
-                               x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], do["topk"], ws_t, ws_t_b)
+                               x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], do["topk"], ws_t, ws_t_b, score_dtype=sdt)
             lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, di["q"], x["k_c"], x["v_c"], lib.BF16, do["topk"],
                                 do["out"], do["lse"], ws_a, ws_a_b)
             comp_done[j].record(stream)
@@ -384,7 +387,8 @@ def run_decode(args, torch, dist, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (indexer) / bf16 (attention)",
         "data": "synthetic",
         "config": {"workload": s.name, "batch_per_gpu": B, "ctx_tokens": s.n, "compressed_entries": Nc,
-                   "indexer": f"{HI}x{dI} e4m3", "top_k": k, "attention": f"{H}x{d} bf16",
+                   "indexer": f"{HI}x{dI} e4m3", "index_scores": args.scores, "top_k": k,
+                   "attention": f"{H}x{d} bf16",
                    "l2": "inputs (5.2 GB per GPU) exceed L2; no flush",
                    "launch": "one step (indexer with fused top-k collection, select, sparse attention) captured "
                              "in a CUDA graph and replayed",

@@ -102,7 +102,10 @@ csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_stream
  *            [B, N_c, d_I / 32].  E2M1 keys are first widened to E4M3 per row:
  *            S = 2^(floor(log2 max_b sc_b) - 5), x8 = E4M3(e * sc_b / S),
  *            sk = S (exact unless e * sc_b / S falls off the E4M3 grid).
- *   scores   device fp32 [B, n_q, N_c].
+ *   scores   device [B, n_q, N_c] in score_dtype: CSA_F32, or CSA_BF16 (the
+ *            fp32 score rounded to nearest even; the score storage precision
+ *            of "DeepSeek-V4 点评总结", FP4 量化感知训练: half the score
+ *            traffic, at a recall cost the tests measure).
  * Precision pairs: (F32, F32) on CUDA cores; (BF16, BF16) and
  * (E4M3, E4M3 | E2M1) on tcgen05 tensor cores with fp32 accumulation, which
  * require H_I = 64 and d_I = 128.
@@ -111,23 +114,25 @@ size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dt
 csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
                               const void* q_idx, csa_dtype_t q_dtype, const float* q_scale,
                               const void* k_idx, csa_dtype_t k_dtype, const void* k_scale,
-                              float* scores, void* workspace, size_t workspace_bytes,
-                              csa_stream_t stream);
+                              void* scores, csa_dtype_t score_dtype, void* workspace,
+                              size_t workspace_bytes, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * csa_topk_select -- top-k selection ("DeepSeek V4 技术解读" §2.1: keep the k
  * best-scoring compressed entries).  Row (b, i) ranks its nv(q_pos0 + i)
  * visible scores by (score descending, index ascending), -0 equal to +0, and
  * writes the first min(k, nv) indices in ascending order, padded with -1.
- * Exact radix selection on the fp32 bit patterns.
- *   scores   device fp32 [B, n_q, N_c];  topk  device int32 [B, n_q, k].
+ * Exact radix selection on the bit patterns of the stored scores.
+ *   scores   device [B, n_q, N_c] in score_dtype (CSA_F32 or CSA_BF16; the
+ *            ranking is that of the stored values, so bf16 ties go to the
+ *            smaller index);  topk  device int32 [B, n_q, k].
  * Requirements: 1 <= k <= 4096, N_c <= 524288, and B * n_q (times
  * ceil(N_c / 32768) for rows longer than 32,768 entries) at most INT_MAX;
  * otherwise CSA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------- */
 size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k);
 csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int k,
-                             const float* scores, int32_t* topk,
+                             const void* scores, csa_dtype_t score_dtype, int32_t* topk,
                              void* workspace, size_t workspace_bytes, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
@@ -138,7 +143,8 @@ csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int
  * cudaMalloc, which can synchronise the device, is not acceptable.  The
  * method's description has no counterpart of this call; it is an addition of
  * this library.
- *   Arguments and results as in csa_topk_select, without the workspace.
+ *   Arguments and results as in csa_topk_select with fp32 scores, without
+ *   the workspace.
  *   Scratch: a fixed device array of CSA_TOPK_NOALLOC_SCRATCH_BYTES (4 MiB)
  *   inside the library.  Rows longer than 32,768 entries need 8 * max(8192,
  *   4k) bytes of it each, plus a few bytes (csa_topk_select_workspace_size
@@ -159,15 +165,20 @@ csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, int m, int 
 /* ---------------------------------------------------------------------------
  * csa_index_topk -- scores and selection in one call (csa_index_scores then
  * csa_topk_select), processing the queries in chunks so that the score
- * buffer stays within the workspace.  Arguments as above.
+ * buffer (score_dtype, in the workspace) stays within 256 MB.  Arguments as
+ * above.  For fewer than four queries a sequence over rows longer than
+ * 32,768 entries (decode), the tensor-core indexer also writes the largest
+ * score of every 32 consecutive entries, and the selection takes its
+ * collection threshold from them (the k-th largest has at least k entries at
+ * or above it) instead of from a sample of the row.
  * ------------------------------------------------------------------------- */
 size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, int k,
-                                     csa_dtype_t k_dtype);
+                                     csa_dtype_t k_dtype, csa_dtype_t score_dtype);
 csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
                             int k, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale,
                             const void* k_idx, csa_dtype_t k_dtype, const void* k_scale,
-                            int32_t* topk, void* workspace, size_t workspace_bytes,
-                            csa_stream_t stream);
+                            csa_dtype_t score_dtype, int32_t* topk, void* workspace,
+                            size_t workspace_bytes, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * csa_sparse_attn -- CSA core attention ("DeepSeek V4 技术解读" §2.1 Core

@@ -105,10 +105,10 @@ size_t scores_ws_bytes(int B, int N_c, int d_I, csa_dtype_t k_dtype)
 }
 
 // Queries per chunk of csa_index_topk: bounded score buffer (multiple of 4).
-int index_chunk_rows(int B, int n_q, int N_c)
+int index_chunk_rows(int B, int n_q, int N_c, size_t score_bytes = 4)
 {
     const size_t budget = 256ull << 20;
-    size_t per_row = (size_t)B * (size_t)(N_c > 0 ? N_c : 1) * 4;
+    size_t per_row = (size_t)B * (size_t)(N_c > 0 ? N_c : 1) * score_bytes;
     long long rows = (long long)(budget / per_row);
     if (rows < 4) rows = 4;
     rows &= ~3ll;
@@ -135,13 +135,13 @@ SplitPlan attn_split_plan(int n_q, long long set_len)
 // maxima there (the top-k's collection threshold).
 csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos0, int m, int N_c, int H_I,
                         int d_I, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
-                        csa_dtype_t k_dtype, const void* k_scale, float* scores, void* ws, cudaStream_t s,
+                        csa_dtype_t k_dtype, const void* k_scale, void* scores, bool sbf16, void* ws, cudaStream_t s,
                         uint32_t* wmax = nullptr, int wmax_ld = 0)
 {
     if (q_dtype == CSA_F32) {
         return cuda_status(launch_indexer_f32(reinterpret_cast<const float*>(q_idx), q_scale,
                                               reinterpret_cast<const float*>(k_idx),
-                                              reinterpret_cast<const float*>(k_scale), scores, B, n_q, i_start,
+                                              reinterpret_cast<const float*>(k_scale), scores, sbf16, B, n_q, i_start,
                                               n_q_rows, q_pos0, m, N_c, H_I, d_I, s),
                            "indexer_f32 launch");
     }
@@ -169,8 +169,8 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos
     if (st != CSA_OK) return st;
     st = make_map(&tk, keys, dt, (uint64_t)d_I, (uint64_t)B * N_c, (uint64_t)d_I * elem, box_inner, 128);
     if (st != CSA_OK) return st;
-    return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, ksc, scores, B, n_q, i_start, n_q_rows, q_pos0, m,
-                                         N_c, num_sms(), wmax, wmax_ld, s),
+    return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, ksc, scores, sbf16, B, n_q, i_start, n_q_rows,
+                                         q_pos0, m, N_c, num_sms(), wmax, wmax_ld, s),
                        "indexer_tc launch");
 }
 
@@ -341,6 +341,12 @@ static csa_status_t check_index_args(int B, int n_q, int64_t q_pos0, int m, int 
     return CSA_OK;
 }
 
+static csa_status_t check_score_dtype(csa_dtype_t t)
+{
+    if (t != CSA_F32 && t != CSA_BF16) return fail(CSA_ERR_UNSUPPORTED, "scores must be F32 or BF16 (got %d)", (int)t);
+    return CSA_OK;
+}
+
 static csa_status_t check_topk(int N_c, int k)
 {
     if (!topk_supported(N_c, k)) return fail(CSA_ERR_UNSUPPORTED, "top-k needs 1 <= k <= 4096, N_c <= 524288 (k=%d, N_c=%d)", k, N_c);
@@ -436,10 +442,12 @@ size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dt
 
 csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, const void* q_idx,
                               csa_dtype_t q_dtype, const float* q_scale, const void* k_idx, csa_dtype_t k_dtype,
-                              const void* k_scale, float* scores, void* workspace, size_t workspace_bytes,
-                              csa_stream_t stream)
+                              const void* k_scale, void* scores, csa_dtype_t score_dtype, void* workspace,
+                              size_t workspace_bytes, csa_stream_t stream)
 {
     csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale);
+    if (st != CSA_OK) return st;
+    st = check_score_dtype(score_dtype);
     if (st != CSA_OK) return st;
     if ((long long)B * n_q * N_c == 0) return CSA_OK;
     if (!scores || !aligned16(scores)) return fail(CSA_ERR_ALIGNMENT, "scores NULL or not aligned");
@@ -447,7 +455,7 @@ csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, in
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     return run_scores(B, n_q, 0, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                      scores, workspace, reinterpret_cast<cudaStream_t>(stream));
+                      scores, score_dtype == CSA_BF16, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k)
@@ -457,11 +465,14 @@ size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k)
 }
 
 
-csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int k, const float* scores,
-                             int32_t* topk, void* workspace, size_t workspace_bytes, csa_stream_t stream)
+csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int k, const void* scores,
+                             csa_dtype_t score_dtype, int32_t* topk, void* workspace, size_t workspace_bytes,
+                             csa_stream_t stream)
 {
     if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes");
     csa_status_t st = check_topk(N_c, k);
+    if (st != CSA_OK) return st;
+    st = check_score_dtype(score_dtype);
     if (st != CSA_OK) return st;
     const long long rows = (long long)B * n_q;
     if (rows == 0) return CSA_OK;
@@ -471,41 +482,47 @@ csa_status_t csa_topk_select(int B, int n_q, int64_t q_pos0, int m, int N_c, int
     const size_t need = topk_workspace_bytes(rows, N_c, k);
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
-    return cuda_status(launch_topk(scores, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, workspace,
+    return cuda_status(launch_topk(scores, score_dtype == CSA_BF16, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, workspace,
                                    reinterpret_cast<cudaStream_t>(stream)),
                        "topk launch");
 }
 
-size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, int k, csa_dtype_t k_dtype)
+size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, int k, csa_dtype_t k_dtype,
+                                     csa_dtype_t score_dtype)
 {
     if (B < 0 || n_q < 0 || N_c < 0 || k < 1) return 0;
-    const int rows = index_chunk_rows(B, n_q, N_c);
-    return align_up((size_t)B * rows * N_c * 4, 256) + scores_ws_bytes(B, N_c, d_I, k_dtype) +
+    const size_t esz = score_dtype == CSA_BF16 ? 2 : 4;
+    const int rows = index_chunk_rows(B, n_q, N_c, esz);
+    return align_up((size_t)B * rows * N_c * esz, 256) + scores_ws_bytes(B, N_c, d_I, k_dtype) +
            topk_workspace_bytes((long long)B * rows, N_c, k) +
            (topk_long_rows(N_c, k) ? topk_wmax_bytes((long long)B * rows, N_c) : 0);
 }
 
 csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
                             const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
-                            csa_dtype_t k_dtype, const void* k_scale, int32_t* topk, void* workspace,
-                            size_t workspace_bytes, csa_stream_t stream)
+                            csa_dtype_t k_dtype, const void* k_scale, csa_dtype_t score_dtype, int32_t* topk,
+                            void* workspace, size_t workspace_bytes, csa_stream_t stream)
 {
     csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale);
     if (st != CSA_OK) return st;
     st = check_topk(N_c, k);
     if (st != CSA_OK) return st;
+    st = check_score_dtype(score_dtype);
+    if (st != CSA_OK) return st;
+    const bool sbf16 = score_dtype == CSA_BF16;
+    const size_t esz = sbf16 ? 2 : 4;
     if ((long long)B * n_q == 0) return CSA_OK;
-    if (!topk_rows_ok((long long)B * index_chunk_rows(B, n_q, N_c), N_c, k))
+    if (!topk_rows_ok((long long)B * index_chunk_rows(B, n_q, N_c, esz), N_c, k))
         return fail(CSA_ERR_UNSUPPORTED, "top-k over %d sequences exceeds the grid limit", B);
     if (!topk || !aligned16(topk)) return fail(CSA_ERR_ALIGNMENT, "topk NULL or not aligned");
-    const size_t need = csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype);
+    const size_t need = csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype, score_dtype);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int rows = index_chunk_rows(B, n_q, N_c);
+    const int rows = index_chunk_rows(B, n_q, N_c, esz);
     uint8_t* w = reinterpret_cast<uint8_t*>(workspace);
-    float* scores = reinterpret_cast<float*>(w);
-    uint8_t* w_scores_ws = w + align_up((size_t)B * rows * N_c * 4, 256);
+    void* scores = w;
+    uint8_t* w_scores_ws = w + align_up((size_t)B * rows * N_c * esz, 256);
     uint8_t* w_topk = w_scores_ws + scores_ws_bytes(B, N_c, d_I, k_dtype);
     uint32_t* w_wmax = reinterpret_cast<uint32_t*>(w_topk + topk_workspace_bytes((long long)B * rows, N_c, k));
     for (int i0 = 0; i0 < n_q; i0 += rows) {
@@ -515,20 +532,20 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
             // with its collection threshold taken from them
             const int ld = topk_wmax_ld(N_c);
             st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                            scores, w_scores_ws, s, w_wmax, ld);
+                            scores, sbf16, w_scores_ws, s, w_wmax, ld);
             if (st != CSA_OK) return st;
-            st = cuda_status(launch_topk(scores, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk,
-                                         s, w_wmax, ld),
+            st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q,
+                                         w_topk, s, w_wmax, ld),
                              "topk launch");
             if (st != CSA_OK) return st;
             continue;
         }
         if (N_c > 0) {
             st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                            scores, w_scores_ws, s);
+                            scores, sbf16, w_scores_ws, s);
             if (st != CSA_OK) return st;
         }
-        st = cuda_status(launch_topk(scores, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk, s),
+        st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk, s),
                          "topk launch");
         if (st != CSA_OK) return st;
     }

@@ -61,10 +61,11 @@ template <bool FP8, int T> struct Cfg {
 // Score of one (key, token): the head sum sum_h sq[h] * acc[h] over the 64
 // accumulator columns (lo = heads 0-31, hi = heads 32-63) with paired FMAs,
 // times the key scale; stored if key < nv (the token's visible entries; -1
-// for a token past the end of the rows).
+// for a token past the end of the rows) as fp32, or rounded to bf16 (nearest
+// even) when sbf16.  Returns the stored value.
 __device__ __forceinline__ float idx_store_score(const uint32_t (&lo)[32], const uint32_t (&hi)[32],
                                                  const float* __restrict__ sq, float sk, int key, int nv,
-                                                 float* __restrict__ srow_ptr)
+                                                 void* __restrict__ srow_ptr, bool sbf16)
 {
     const float4* sq4 = reinterpret_cast<const float4*>(sq);
     uint64_t pa = 0, pb = 0, pc = 0, pd = 0;   // packed partial sums (x, y halves)
@@ -78,8 +79,14 @@ __device__ __forceinline__ float idx_store_score(const uint32_t (&lo)[32], const
         pd = ffma2(pack_f32x2(u4.z, u4.w), pack_u32x2(hi[4 * h4 + 2], hi[4 * h4 + 3]), pd);
     }
     const float2 fa = unpack_f32x2(pa), fb = unpack_f32x2(pb), fc = unpack_f32x2(pc), fd = unpack_f32x2(pd);
-    const float sc = (((fa.x + fa.y) + (fb.x + fb.y)) + ((fc.x + fc.y) + (fd.x + fd.y))) * sk;
-    if (key < nv) srow_ptr[key] = sc;
+    float sc = (((fa.x + fa.y) + (fb.x + fb.y)) + ((fc.x + fc.y) + (fd.x + fd.y))) * sk;
+    if (sbf16) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(sc);
+        if (key < nv) reinterpret_cast<__nv_bfloat16*>(srow_ptr)[key] = h;
+        sc = __bfloat162float(h);
+    } else if (key < nv) {
+        reinterpret_cast<float*>(srow_ptr)[key] = sc;
+    }
     return sc;
 }
 
@@ -93,8 +100,8 @@ __device__ __forceinline__ float idx_store_score(const uint32_t (&lo)[32], const
 template <bool FP8, int T, bool WMAX>
 __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-    const float* __restrict__ q_scale, const float* __restrict__ k_scale, float* __restrict__ scores,
-    int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int n_splits,
+    const float* __restrict__ q_scale, const float* __restrict__ k_scale, void* __restrict__ scores,
+    int score_bf16, int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int n_splits,
     int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
 {
     using C = idx::Cfg<FP8, T>;
@@ -229,7 +236,9 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             const long long nvl_t = (q_pos0 + i_start + i_tok + 1) / m;
             nv_tok = (int)(nvl_t < Nc ? nvl_t : Nc);
         }
-        float* const srow_ptr = scores + ((long long)b * n_q_rows + (i_tok < n_q_rows ? i_tok : 0)) * Nc;
+        const bool sbf16 = score_bf16 != 0;
+        void* const srow_ptr = reinterpret_cast<uint8_t*>(scores) +
+                               ((long long)b * n_q_rows + (i_tok < n_q_rows ? i_tok : 0)) * Nc * (sbf16 ? 2 : 4);
         for (int li = 0; li < n_tiles; ++li) {
             const int acc = li % C::ACC;
             const int key = (tile0 + li) * idx::BLOCK_KEYS + row;
@@ -246,7 +255,7 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_acc_empty[acc]);
-            const float sc = idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr);
+            const float sc = idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr, sbf16);
             if constexpr (WMAX) {
                 const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, key < nv_tok ? score_key(sc) : 0u);
                 const int grp = (tile0 + li) * (idx::BLOCK_KEYS / 32) + quad;   // keys 32 grp .. 32 grp + 31
@@ -269,7 +278,7 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) indexer_f32_kernel(
     const float* __restrict__ q, const float* __restrict__ q_scale, const float* __restrict__ k,
-    const float* __restrict__ k_scale, float* __restrict__ scores, int n_q_total, int i_start,
+    const float* __restrict__ k_scale, void* __restrict__ scores, int score_bf16, int n_q_total, int i_start,
     int n_q_rows, long long q_pos0, int m, int Nc, int HI, int dI)
 {
     extern __shared__ float qs[];
@@ -293,7 +302,8 @@ __global__ void __launch_bounds__(256) indexer_f32_kernel(
         const float sq = q_scale ? qs[HI * dI + h] : 1.f;
         s = fmaf(sq * sk, dot, s);
     }
-    scores[(long long)r * Nc + j] = s;
+    if (score_bf16) reinterpret_cast<__nv_bfloat16*>(scores)[(long long)r * Nc + j] = __float2bfloat16_rn(s);
+    else reinterpret_cast<float*>(scores)[(long long)r * Nc + j] = s;
 }
 
 // ---------------------------------------------------------------------------
@@ -349,7 +359,7 @@ cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t
 }
 
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
-                               float* scores, int B, int n_q_total, int i_start, int n_q_rows,
+                               void* scores, bool score_bf16, int B, int n_q_total, int i_start, int n_q_rows,
                                long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s)
 {
     if (B * n_q_rows == 0 || Nc == 0) return cudaSuccess;
@@ -357,14 +367,14 @@ cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float
     size_t smem = (size_t)(HI * dI + HI) * sizeof(float);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(indexer_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    indexer_f32_kernel<<<grid, 256, smem, s>>>(q, q_scale, k, k_scale, scores, n_q_total, i_start,
-                                               n_q_rows, q_pos0, m, Nc, HI, dI);
+    indexer_f32_kernel<<<grid, 256, smem, s>>>(q, q_scale, k, k_scale, scores, score_bf16 ? 1 : 0, n_q_total,
+                                               i_start, n_q_rows, q_pos0, m, Nc, HI, dI);
     return cudaGetLastError();
 }
 
 template <bool FP8, int T, bool WMAX>
 static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const float* q_scale,
-                             const float* k_scale, float* scores, int B, int n_q_total, int i_start,
+                             const float* k_scale, void* scores, bool score_bf16, int B, int n_q_total, int i_start,
                              int n_q_rows, long long q_pos0, int m, int Nc, int num_sms, uint32_t* wmax,
                              int wmax_ld, cudaStream_t s)
 {
@@ -383,27 +393,27 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     auto kern = indexer_tc_kernel<FP8, T, WMAX>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     dim3 grid(n_groups * splits, B);
-    kern<<<grid, idx::threads<T>(), C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, n_q_total, i_start, n_q_rows,
-                                             q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
+    kern<<<grid, idx::threads<T>(), C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, score_bf16 ? 1 : 0, n_q_total,
+                                             i_start, n_q_rows, q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
     return cudaGetLastError();
 }
 
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const float* q_scale, const float* k_scale, float* scores, int B,
+                              const float* q_scale, const float* k_scale, void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
                               int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s)
 {
     if (wmax) {   // decode groups (T = 1) only
         if (T != 1) return cudaErrorInvalidValue;
-        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
-        return launch_tc<false, 1, true>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        return launch_tc<false, 1, true>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
     }
     if (fp8) {
-        if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
-        return launch_tc<true, 1, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+        if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+        return launch_tc<true, 1, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
     }
-    if (T == 4) return launch_tc<false, 4, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
-    return launch_tc<false, 1, false>(tq, tk, q_scale, k_scale, scores, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+    if (T == 4) return launch_tc<false, 4, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+    return launch_tc<false, 1, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
 }
 
 int indexer_group_tokens(int n_q) { return n_q >= 4 ? 4 : 1; }

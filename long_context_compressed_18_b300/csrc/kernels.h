@@ -42,7 +42,8 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k);
 // largest score key of every run of 32 consecutive entries (wmax_ld words a
 // row), written by the decode indexer; the collection then takes its
 // threshold from them instead of from a sample of the row.
-cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
+// scores: fp32, or bf16 when scores_bf16 (selection on the stored values).
+cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, long long q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
                         cudaStream_t s, const uint32_t* wmax = nullptr, int wmax_ld = 0);
 bool topk_long_rows(int N_c, int k);
@@ -55,12 +56,13 @@ int indexer_box_rows(int T);
 // wmax non-null (decode groups, T = 1): the epilogue also writes, per row
 // (b * n_q_rows + i of the chunk), the largest score key (score_key) of every
 // 32 consecutive visible entries j to wmax[row * wmax_ld + j / 32].
+// scores: fp32, or bf16 (nearest even) when score_bf16.
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const float* q_scale, const float* k_scale, float* scores, int B,
+                              const float* q_scale, const float* k_scale, void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
                               int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s);
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
-                               float* scores, int B, int n_q_total, int i_start, int n_q_rows,
+                               void* scores, bool score_bf16, int B, int n_q_total, int i_start, int n_q_rows,
                                long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s);
 cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t* x8, float* S,
                                long long rows, int d, cudaStream_t s);

@@ -23,6 +23,35 @@ namespace csa {
 constexpr int TOPK_THREADS = 512;
 constexpr int TOPK_WARPS = TOPK_THREADS / 32;
 
+// Scores are stored as fp32 or bf16 (ST); every load widens them to fp32
+// exactly, so the keys -- and the selection -- are those of the stored values.
+// at4 reads four consecutive scores (16 bytes of fp32, 8 of bf16) from a
+// pointer aligned to their size (aligned4).
+template <typename ST> struct ScoreIO;
+template <> struct ScoreIO<float> {
+    static __device__ __forceinline__ float at(const float* p, long long i) { return __ldg(p + i); }
+    static __device__ __forceinline__ float4 at4(const float* p, long long i4)
+    {
+        return __ldg(reinterpret_cast<const float4*>(p) + i4);
+    }
+};
+template <> struct ScoreIO<__nv_bfloat16> {
+    static __device__ __forceinline__ float at(const __nv_bfloat16* p, long long i)
+    {
+        return bf16_bits_to_f32(__ldg(reinterpret_cast<const unsigned short*>(p) + i));
+    }
+    static __device__ __forceinline__ float4 at4(const __nv_bfloat16* p, long long i4)
+    {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + i4);
+        return make_float4(bf16_bits_to_f32(u.x & 0xFFFFu), bf16_bits_to_f32(u.x >> 16),
+                           bf16_bits_to_f32(u.y & 0xFFFFu), bf16_bits_to_f32(u.y >> 16));
+    }
+};
+template <typename ST> __device__ __forceinline__ bool aligned4(const ST* p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (4 * sizeof(ST) - 1)) == 0;
+}
+
 // Radix levels over the 32-bit key: bits 31..21 (2048 bins), 20..10 (2048),
 // 9..0 (1024).  The first level's histogram is built while the scores are
 // loaded; the second while the elements of the selected first-level bin are
@@ -133,19 +162,19 @@ __device__ void radix_threshold(const uint32_t* keys, int len, int kk, TopkShare
 
 // Loads len fp32 scores into shared memory as keys and accumulates the
 // first-level histogram.  Each thread keeps eight loads in flight.
-__device__ void load_score_keys(const float* __restrict__ src, int len, uint32_t* keys, TopkShared& sh)
+template <typename ST>
+__device__ void load_score_keys(const ST* __restrict__ src, int len, uint32_t* keys, TopkShared& sh)
 {
     const int tid = threadIdx.x;
     constexpr int U = 8;
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    if (aligned4(src)) {
         const int n4 = len >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(src);
         for (int base = 0; base < n4; base += TOPK_THREADS * U) {
             float4 f[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int v = base + u * TOPK_THREADS + tid;
-                f[u] = v < n4 ? __ldg(s4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+                f[u] = v < n4 ? ScoreIO<ST>::at4(src, v) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -162,7 +191,7 @@ __device__ void load_score_keys(const float* __restrict__ src, int len, uint32_t
             }
         }
         for (int e = 4 * n4 + tid; e < len; e += TOPK_THREADS) {
-            const uint32_t key = score_key(__ldg(src + e));
+            const uint32_t key = score_key(ScoreIO<ST>::at(src, e));
             keys[e] = key;
             atomicAdd(&sh.hist[key >> 21], 1u);
         }
@@ -172,7 +201,7 @@ __device__ void load_score_keys(const float* __restrict__ src, int len, uint32_t
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int e = base + u * TOPK_THREADS + tid;
-                f[u] = e < len ? __ldg(src + e) : 0.f;
+                f[u] = e < len ? ScoreIO<ST>::at(src, e) : 0.f;
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -237,8 +266,9 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
 // Rows of at most TOPK_SMEM_ROW entries: one CTA per row, the row's keys staged
 // in shared memory, one radix select over them and an ordered compaction;
 // writes the final indices, -1 padded.
+template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc,
     int k, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -326,22 +356,21 @@ __device__ __forceinline__ int visible_len(long long q_pos0, int i, int m, int N
 // Streams score keys [c0, c0 + len) of a row: f(in_range, index, key) is
 // called the same number of times in every lane (callers use warp ballots).
 // 16-byte vector loads when the start is aligned, eight loads in flight.
-template <typename F>
-__device__ __forceinline__ void stream_keys(const float* __restrict__ row, int c0, int len, F f)
+template <typename ST, typename F>
+__device__ __forceinline__ void stream_keys(const ST* __restrict__ row, int c0, int len, F f)
 {
     constexpr int U = 8;
     const int tid = threadIdx.x;
-    const float* src = row + c0;
+    const ST* src = row + c0;
     int done = 0;
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    if (aligned4(src)) {
         const int n4 = len >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(src);
         for (int base = 0; base < n4; base += TOPK_THREADS * U) {
             float4 v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int e4 = base + u * TOPK_THREADS + tid;
-                v[u] = e4 < n4 ? __ldg(s4 + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[u] = e4 < n4 ? ScoreIO<ST>::at4(src, e4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -361,7 +390,7 @@ __device__ __forceinline__ void stream_keys(const float* __restrict__ row, int c
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = base + u * TOPK_THREADS + tid;
-            v[u] = e < len ? __ldg(src + e) : 0.f;
+            v[u] = e < len ? ScoreIO<ST>::at(src, e) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -380,8 +409,8 @@ __device__ __forceinline__ void stream_keys(const float* __restrict__ row, int c
 // within the selected bin) locate rank t, and the lowest key whose spread key
 // falls in that second-level bin is returned.  keys: shared buffer of smax
 // entries.
-template <int SMAX>
-__device__ uint32_t sample_threshold(const float* __restrict__ row, int L, int kk, uint32_t* keys, TopkShared& sh)
+template <int SMAX, typename ST>
+__device__ uint32_t sample_threshold(const ST* __restrict__ row, int L, int kk, uint32_t* keys, TopkShared& sh)
 {
     const int S = L < SMAX ? L : SMAX;
     const int runs = S / 32 > 0 ? S / 32 : 1;
@@ -397,7 +426,7 @@ __device__ uint32_t sample_threshold(const float* __restrict__ row, int L, int k
         const int q = u * TOPK_THREADS + tid;
         const int run = q >> 5;
         const int e = (L < SMAX) ? q : (int)(((uint64_t)run * step) >> 8) + (q & 31);
-        v[u] = q < S ? __ldg(row + e) : 0.f;
+        v[u] = q < S ? ScoreIO<ST>::at(row, e) : 0.f;
     }
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
@@ -463,13 +492,14 @@ __device__ __forceinline__ float key_value(uint32_t k)
 // NaN, exactly like the keys; a threshold key of 0 takes every entry.  Each
 // thread builds a take mask over its batch of loads; one warp scan and one
 // shared atomic per batch place the entries.
-__device__ void collect_entries(const float* __restrict__ row, int c0, int len, uint32_t thr, uint32_t* lkey,
+template <typename ST>
+__device__ void collect_entries(const ST* __restrict__ row, int c0, int len, uint32_t thr, uint32_t* lkey,
                                 int32_t* lidx, uint32_t cap, uint32_t* n_loc)
 {
     const bool take_all = thr == 0u;
     const float tf = key_value(thr);
     const int tid = threadIdx.x, lane = tid & 31;
-    const float* src = row + c0;
+    const ST* src = row + c0;
     auto reserve = [&](uint32_t n) -> uint32_t {
         uint32_t incl = n;
 #pragma unroll
@@ -492,14 +522,14 @@ __device__ void collect_entries(const float* __restrict__ row, int c0, int len, 
     };
     constexpr int U = 8;
     int done = 0;
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    if (aligned4(src)) {
         const int n4 = len >> 2;
         for (int base = 0; base < n4; base += TOPK_THREADS * U) {
             float4 f[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int e4 = base + u * TOPK_THREADS + tid;
-                f[u] = e4 < n4 ? __ldg(reinterpret_cast<const float4*>(src) + e4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                f[u] = e4 < n4 ? ScoreIO<ST>::at4(src, e4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             uint32_t mask = 0;
 #pragma unroll
@@ -531,7 +561,7 @@ __device__ void collect_entries(const float* __restrict__ row, int c0, int len, 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = base + u * TOPK_THREADS + tid;
-            v[u] = e < len ? __ldg(src + e) : 0.f;
+            v[u] = e < len ? ScoreIO<ST>::at(src, e) : 0.f;
         }
         uint32_t mask = 0;
 #pragma unroll
@@ -568,8 +598,9 @@ __device__ uint32_t wmax_threshold(const uint32_t* __restrict__ wrow, int nw, in
     return T;
 }
 
+template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
     int n_chunks, LongRowWs w, const uint32_t* __restrict__ wmax, int wmax_ld)
 {
     // the chunk's entries go to a shared-memory list, then one global atomic
@@ -775,7 +806,8 @@ __device__ void select_entries(uint32_t* ekey, const int32_t* eidx, int n, int k
 
 // Exact selection of a row's top kk streamed from global memory: the three
 // radix levels, then the ordered compaction.
-__device__ void select_streaming(const float* __restrict__ row, int L, int kk, TopkShared& sh,
+template <typename ST>
+__device__ void select_streaming(const ST* __restrict__ row, int L, int kk, TopkShared& sh,
                                  int32_t* __restrict__ o)
 {
     clear_hist(sh, 2048);
@@ -805,12 +837,13 @@ __device__ void select_streaming(const float* __restrict__ row, int L, int kk, T
     find_bin<1024>(sh, rem);
     const uint32_t T = (pre << 10) | sh.bin;
     const int teq = (int)(rem - sh.above);
-    ordered_compact_by([&](int e) { return score_key(__ldg(row + e)); }, L, T, teq, sh,
+    ordered_compact_by([&](int e) { return score_key(ScoreIO<ST>::at(row, e)); }, L, T, teq, sh,
                        [&](int pos, int e) { if (pos < kk) o[pos] = e; });
 }
 
+template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
     LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -827,7 +860,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
         for (int e = tid; e < L; e += TOPK_THREADS) o[e] = e;
         return;
     }
-    const float* row = scores + (long long)r * ld;
+    const ST* row = scores + (long long)r * ld;
     const uint32_t got = __ldcg(w.cnt + r);
     if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
         uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem_raw);   // two bitmaps of the row
@@ -879,8 +912,9 @@ static int row_cap(int N_c, int k)
 
 static size_t row_smem_bytes(int N_c, int k) { return (size_t)row_cap(N_c, k) * 8 + (size_t)2 * bitmap_words(N_c) * 4; }
 
+template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
-    const float* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k, int cap,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k, int cap,
     int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -901,7 +935,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
         for (int e = tid; e < L; e += TOPK_THREADS) o[e] = e;
         return;
     }
-    const float* row = scores + (long long)r * ld;
+    const ST* row = scores + (long long)r * ld;
     const uint32_t thr = L > cap ? sample_threshold<ROW_SAMPLES>(row, L, kk, ekey, sh) : 0u;   // 0: take all
     if (tid == 0) n_cnt = 0;
     __syncthreads();
@@ -949,22 +983,24 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k)
 // The select kernel over a row's entry list.  The fast route needs two
 // bitmaps of the row and the entry list in shared memory; shapes beyond that
 // stream every row instead.
-static cudaError_t launch_select(const float* scores, long long ld, int n_q_rows, long long q_pos0, int m, int N_c,
+template <typename ST>
+static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, long long q_pos0, int m, int N_c,
                                  int k, const LongRowWs& w, int rows, int32_t* out, long long out_b_stride,
                                  cudaStream_t s)
 {
     size_t smem = (size_t)2 * bitmap_words(N_c) * 4 + (size_t)w.cap * 8;
     const int fast_ok = smem <= (size_t)200 * 1024;
     if (!fast_ok) smem = 0;
-    cudaFuncSetAttribute(topk_lr_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    topk_lr_select_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok, out,
-                                                          out_b_stride);
+    auto kern = topk_lr_select_kernel<ST>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok, out, out_b_stride);
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, long long q_pos0,
-                        int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
-                        cudaStream_t s, const uint32_t* wmax, int wmax_ld)
+template <typename ST>
+static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_rows, long long q_pos0, int m,
+                                 int N_c, int k, int32_t* out, long long out_b_stride, void* ws, cudaStream_t s,
+                                 const uint32_t* wmax, int wmax_ld)
 {
     const long long rows_ll = (long long)B * n_q_rows;
     if (rows_ll == 0) return cudaSuccess;
@@ -973,25 +1009,39 @@ cudaError_t launch_topk(const float* scores, long long ld, int B, int n_q_rows, 
     TopkPlan p = topk_plan(N_c, k);
     if (p.n_chunks == 1 && N_c <= TOPK_SMEM_ROW) {
         const size_t smem = (size_t)(N_c > 0 ? N_c : 1) * sizeof(uint32_t);
-        cudaFuncSetAttribute(topk_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        topk_smem_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
+        auto kern = topk_smem_kernel<ST>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
         return cudaGetLastError();
     }
     if (p.n_chunks == 1) {
         const size_t smem = row_smem_bytes(N_c, k);
-        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        topk_kernel<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, row_cap(N_c, k), out,
-                                                     out_b_stride);
+        auto kern = topk_kernel<ST>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, row_cap(N_c, k), out,
+                                              out_b_stride);
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
     cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)rows * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
-    cudaFuncSetAttribute(topk_lr_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-    topk_lr_collect_kernel<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k,
-                                                                          p.n_chunks, w, wmax, wmax_ld);
+    auto ckern = topk_lr_collect_kernel<ST>;
+    cudaFuncSetAttribute(ckern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+    ckern<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, p.n_chunks, w,
+                                                        wmax, wmax_ld);
     return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, rows, out, out_b_stride, s);
+}
+
+cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, long long q_pos0,
+                        int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
+                        cudaStream_t s, const uint32_t* wmax, int wmax_ld)
+{
+    if (scores_bf16)
+        return launch_topk_t(reinterpret_cast<const __nv_bfloat16*>(scores), ld, B, n_q_rows, q_pos0, m, N_c, k, out,
+                             out_b_stride, ws, s, wmax, wmax_ld);
+    return launch_topk_t(reinterpret_cast<const float*>(scores), ld, B, n_q_rows, q_pos0, m, N_c, k, out,
+                         out_b_stride, ws, s, wmax, wmax_ld);
 }
 
 bool topk_long_rows(int N_c, int k) { return topk_plan(N_c, k).n_chunks > 1; }

@@ -70,7 +70,7 @@ extern "C" csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, 
     }
     // The per-row counters must start at zero: launch_topk clears them on
     // the stream (one memset) before the long-row kernels use them.
-    const cudaError_t e = csa::launch_topk(scores, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, scratch,
+    const cudaError_t e = csa::launch_topk(scores, false, N_c, B, n_q, q_pos0, m, N_c, k, topk, n_q, scratch,
                                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return csa::report(CSA_ERR_CUDA, cudaGetErrorString(e));
     return CSA_OK;

@@ -48,12 +48,12 @@ def load():
     sig = {
         "csa_compress": ([_I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P], _I),
         "csa_index_scores_workspace_size": ([_I, _I, _I, _I], _S),
-        "csa_index_scores": ([_I, _I, _L, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _S, _P], _I),
+        "csa_index_scores": ([_I, _I, _L, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _I, _P, _S, _P], _I),
         "csa_topk_select_workspace_size": ([_I, _I, _I, _I], _S),
-        "csa_topk_select": ([_I, _I, _L, _I, _I, _I, _P, _P, _P, _S, _P], _I),
+        "csa_topk_select": ([_I, _I, _L, _I, _I, _I, _P, _I, _P, _P, _S, _P], _I),
         "csa_topk_select_noalloc": ([_I, _I, _L, _I, _I, _I, _P, _P, _P], _I),
-        "csa_index_topk_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
-        "csa_index_topk": ([_I, _I, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _S, _P], _I),
+        "csa_index_topk_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _S),
+        "csa_index_topk": ([_I, _I, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _I, _P, _P, _S, _P], _I),
         "csa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I], _S),
         "csa_sparse_attn": ([_I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P], _I),
         "hca_attn": ([_I, _I, _L, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
@@ -110,9 +110,10 @@ def csa_index_scores_workspace_size(B, N_c, d_I, k_dtype):
 
 def csa_index_scores(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
                      scores, workspace=None, workspace_bytes=0, stream=None):
+    """scores: an fp32 or bf16 tensor; its dtype is the score_dtype passed on."""
     _check(load().csa_index_scores(B, n_q, q_pos0, m, N_c, H_I, d_I, _ptr(q_idx), q_dtype, _ptr(q_scale),
-                                   _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(scores), _ptr(workspace),
-                                   workspace_bytes, _stream(stream)))
+                                   _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(scores), dtype_code(scores.dtype),
+                                   _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def csa_topk_select_workspace_size(B, n_q, N_c, k):
@@ -120,8 +121,9 @@ def csa_topk_select_workspace_size(B, n_q, N_c, k):
 
 
 def csa_topk_select(B, n_q, q_pos0, m, N_c, k, scores, topk, workspace=None, workspace_bytes=0, stream=None):
-    _check(load().csa_topk_select(B, n_q, q_pos0, m, N_c, k, _ptr(scores), _ptr(topk), _ptr(workspace),
-                                  workspace_bytes, _stream(stream)))
+    """scores: an fp32 or bf16 tensor; its dtype is the score_dtype passed on."""
+    _check(load().csa_topk_select(B, n_q, q_pos0, m, N_c, k, _ptr(scores), dtype_code(scores.dtype), _ptr(topk),
+                                  _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def csa_topk_select_noalloc(B, n_q, q_pos0, m, N_c, k, scores, topk, stream=None):
@@ -133,14 +135,15 @@ def csa_topk_select_noalloc(B, n_q, q_pos0, m, N_c, k, scores, topk, stream=None
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
-def csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype):
-    return load().csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype)
+def csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype, score_dtype=F32):
+    return load().csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype, score_dtype)
 
 
 def csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                   topk, workspace, workspace_bytes, stream=None):
+                   topk, workspace, workspace_bytes, stream=None, score_dtype=F32):
+    """score_dtype (keyword; F32 or BF16) is the C argument that precedes topk."""
     _check(load().csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, _ptr(q_idx), q_dtype, _ptr(q_scale),
-                                 _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(topk), _ptr(workspace),
+                                 _ptr(k_idx), k_dtype, _ptr(k_scale), score_dtype, _ptr(topk), _ptr(workspace),
                                  workspace_bytes, _stream(stream)))
 
 

@@ -61,13 +61,13 @@ def compress(logits, xs, m: int, out_kinds):
 
 
 def index_topk(q_idx, q_dtype: str, q_scale, k_idx, k_dtype: str, k_scale, q_pos0: int, m: int, N_c: int,
-               k: int, ws: Workspace):
+               k: int, ws: Workspace, score_dtype: str = "f32"):
     B, n_q, H_I, d_I = q_idx.shape[0], q_idx.shape[1], q_idx.shape[2], q_idx.shape[3]
     topk = torch.empty(B, n_q, k, dtype=torch.int32, device=q_idx.device)
-    nbytes = lib.csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, _CODE[k_dtype])
+    nbytes = lib.csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, _CODE[k_dtype], _CODE[score_dtype])
     buf, nb = ws.get(nbytes)
     lib.csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, q_idx, _CODE[q_dtype], q_scale, k_idx,
-                       _CODE[k_dtype], k_scale, topk, buf, nb)
+                       _CODE[k_dtype], k_scale, topk, buf, nb, score_dtype=_CODE[score_dtype])
     return topk
 
 
@@ -110,11 +110,12 @@ def csa_layer(x: dict, s, ws: Workspace):
     return dict(k_c=kc, v_c=vc, idx_k_c=ikc, idx_k_c_scale=iks, topk=topk, out=out, lse=lse)
 
 
-def csa_decode(x: dict, s, ws: Workspace):
+def csa_decode(x: dict, s, ws: Workspace, score_dtype: str = "f32"):
     """One CSA decode step over resident compressed caches: score, select,
-    attend (the headline path)."""
+    attend (the headline path).  score_dtype "bf16" stores the index scores
+    in bf16."""
     topk = index_topk(x["idx_q"], s.idx_q_dtype, x["idx_q_scale"], x["idx_k_c"], s.idx_k_dtype,
-                      x["idx_k_c_scale"], s.q_pos0, s.m, s.N_c, s.k, ws)
+                      x["idx_k_c_scale"], s.q_pos0, s.m, s.N_c, s.k, ws, score_dtype)
     out, lse = sparse_attn(x["q"], x["k_c"], x["v_c"], topk, 1.0 / math.sqrt(s.d), ws)
     return dict(topk=topk, out=out, lse=lse)
 

@@ -42,12 +42,12 @@ def test_host_side_validation_without_gpu():
     st = L.csa_compress(1, 16, 0, None, 1, None, None, None, None, None, None, None)
     assert st == 1 and "m=0" in L.csa_last_error().decode()
     st = L.csa_index_scores(1, 4, 0, 4, 8, 64, 128, None, lib.BF16, None, None, lib.E4M3, None,
-                            None, None, 0, None)
+                            None, lib.F32, None, 0, None)
     assert st == 2
     st = L.csa_index_scores(1, 4, 0, 4, 8, 32, 128, None, lib.BF16, None, None, lib.BF16, None,
-                            None, None, 0, None)
+                            None, lib.F32, None, 0, None)
     assert st == 2 and "H_I=64" in L.csa_last_error().decode()
-    st = L.csa_topk_select(1, 1, 0, 1, 10, 0, None, None, None, 0, None)
+    st = L.csa_topk_select(1, 1, 0, 1, 10, 0, None, lib.F32, None, None, 0, None)
     assert st == 2
     st = L.hca_attn(1, 1, 0, 4, 8, 12, 128, 0.1, None, None, None, lib.BF16, None, None, None)
     assert st == 2
@@ -78,14 +78,14 @@ def test_empty_inputs_and_limits_without_gpu():
     st = L.csa_compress(1, 16, 4, 256, 1, addr, bf, (I * 1)(16), addr, e2, addr, None)
     assert st == 2 and "E2M1" in L.csa_last_error().decode()
     # top-k: k <= 4096, rows <= 524,288 entries, long rows need the workspace
-    assert L.csa_topk_select(1, 1, 0, 4, 1000, 4097, 256, 256, None, 0, None) == 2
-    assert L.csa_topk_select(1, 1, 0, 4, 524289, 16, 256, 256, None, 0, None) == 2
+    assert L.csa_topk_select(1, 1, 0, 4, 1000, 4097, 256, lib.F32, 256, None, 0, None) == 2
+    assert L.csa_topk_select(1, 1, 0, 4, 524289, 16, 256, lib.F32, 256, None, 0, None) == 2
     need = L.csa_topk_select_workspace_size(2, 1, 262144, 1024)
-    st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, 256, None, 0, None)
+    st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, lib.F32, 256, None, 0, None)
     assert st == 4 and str(need) in L.csa_last_error().decode()
-    st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, 256, 256, need - 16, None)
+    st = L.csa_topk_select(2, 1, 4 * 262144 - 1, 4, 262144, 1024, 256, lib.F32, 256, 256, need - 16, None)
     assert st == 4
-    assert L.csa_topk_select(0, 1, 0, 4, 1000, 16, None, None, None, 0, None) == 0
+    assert L.csa_topk_select(0, 1, 0, 4, 1000, 16, None, lib.F32, None, None, 0, None) == 0
 
 
 def test_topk_row_count_is_checked_in_64_bits():
@@ -94,10 +94,10 @@ def test_topk_row_count_is_checked_in_64_bits():
     query computes in 64 bits."""
     L = lib.load()
     B, n_q = 70000, 40000                        # 2.8e9 rows
-    assert L.csa_topk_select(B, n_q, 0, 4, 1000, 16, 256, 256, None, 0, None) == 2
+    assert L.csa_topk_select(B, n_q, 0, 4, 1000, 16, 256, lib.F32, 256, None, 0, None) == 2
     assert "grid limit" in L.csa_last_error().decode()
     assert L.csa_topk_select_noalloc(B, n_q, 0, 4, 1000, 16, 256, 256, None) == 2
     # 2^27 long rows of 16 chunks each exceed INT_MAX CTAs
-    assert L.csa_topk_select(1 << 14, 1 << 13, 4 * 524288 - 1, 4, 524288, 16, 256, 256, None, 0, None) == 2
+    assert L.csa_topk_select(1 << 14, 1 << 13, 4 * 524288 - 1, 4, 524288, 16, 256, lib.F32, 256, None, 0, None) == 2
     need = L.csa_topk_select_workspace_size(65536, 65536, 262144, 1024)
     assert need >= 65536 * 65536 * 8 * 4096      # no 32-bit wraparound
