@@ -41,13 +41,14 @@ def lib():
             "orc_e4m3_encode_array": ([_L, _P, _P], None),
             "orc_e2m1_encode_array": ([_L, _P, _P], None),
             "orc_compress": ([_I, _I, _I, _I, _P, _P, _P], None),
+            "orc_compress_per_channel": ([_I, _I, _I, _I, _P, _P, _P], None),
             "orc_quant_e4m3_rows": ([_L, _I, _P, _P, _P], None),
             "orc_quant_e2m1_blocks": ([_L, _I, _P, _P, _P], None),
             "orc_fp4_to_e4m3": ([_L, _I, _P, _P, _P, _P], _L),
             "orc_index_scores": ([_I, _I, _L, _I, _I, _I, _I, _P, _P, _P, _P,
-                                  _I, _P, _P, _P], None),
+                                  _P, _I, _I, _P, _P, _P], None),
             "orc_topk": ([_I, _P, _L, _I, _P, _P], None),
-            "orc_attention": ([_I, _I, _I, _I, _L, _P, _P, _P, C.c_double, _I,
+            "orc_attention": ([_I, _I, _I, _I, _I, _L, _P, _P, _P, C.c_double, _I,
                                _L, _I, _L, _P, _I, _I, _P, _P, _P], None),
             "orc_num_threads": ([], _I),
         }
@@ -129,6 +130,17 @@ def compress(logits, x, m: int) -> np.ndarray:
     return out
 
 
+def compress_per_channel(logits, x, m: int) -> np.ndarray:
+    """Per-channel weights: [B, n, d] logits, [B, n, d] x -> fp64 [B, n // m, d]."""
+    lg = _np(logits, np.float32)
+    xx = _np(x, np.float32)
+    B, n, d = xx.shape
+    assert lg.shape == xx.shape
+    out = np.empty((B, n // m, d), np.float64)
+    lib().orc_compress_per_channel(B, n, m, d, _ptr(lg), _ptr(xx), _ptr(out))
+    return out
+
+
 def quant_e4m3_rows(x32):
     x = _np(x32, np.float32)
     rows, d = int(np.prod(x.shape[:-1])), x.shape[-1]
@@ -161,10 +173,11 @@ def fp4_to_e4m3(packed, sc_codes):
 # ---- a2: indexer scores -----------------------------------------------------
 
 def index_scores(q_vals, q_scale, k_vals, k_scale, q_pos0: int, m: int,
-                 rows=None):
+                 rows=None, head_w=None, relu: bool = False):
     """q_vals [B, n_q, H_I, d_I] and k_vals [B, N_c, d_I] are the decoded
     stored values.  Returns (fp64 scores, fp32 scores), shape [R, N_c]; NaN
-    where an entry is not visible."""
+    where an entry is not visible.  head_w [B, n_q, H_I] and relu select the
+    weighted / ReLU variant."""
     q = _np(q_vals, np.float32)
     k = _np(k_vals, np.float32)
     B, n_q, HI, dI = q.shape
@@ -175,8 +188,9 @@ def index_scores(q_vals, q_scale, k_vals, k_scale, q_pos0: int, m: int,
     R = B * n_q if rr is None else rr.size
     o64 = np.empty((R, Nc), np.float64)
     o32 = np.empty((R, Nc), np.float32)
+    hw = None if head_w is None else _np(head_w, np.float32)
     lib().orc_index_scores(B, n_q, q_pos0, m, Nc, HI, dI, _ptr(q), _ptr(qs), _ptr(k),
-                           _ptr(ks), 0 if rr is None else rr.size, _ptr(rr),
+                           _ptr(ks), _ptr(hw), 1 if relu else 0, 0 if rr is None else rr.size, _ptr(rr),
                            _ptr(o64), _ptr(o32))
     return o64, o32
 
@@ -203,20 +217,24 @@ SPARSE, CLOSED_BLOCKS, WINDOW = 0, 1, 2
 
 def attention(q, K, V, tau: float, mode: int, q_pos0: int = 0, m: int = 1,
               window: int = 0, idx=None, rows=None):
-    """q [B, n_q, H, d]; K, V [B, N_kv, d].  Returns (out [R, H, d], lse [R, H])
-    in fp64 for the selected flat rows (all rows when ``rows`` is None)."""
+    """q [B, n_q, H, d]; K, V [B, N_kv, d] (one shared KV head) or
+    [B, N_kv, H_kv, d] (query head h reads KV head h // (H // H_kv)).  Returns
+    (out [R, H, d], lse [R, H]) in fp64 for the selected flat rows (all rows
+    when ``rows`` is None)."""
     qq = _np(q, np.float32)
     KK = _np(K, np.float32)
     VV = _np(V, np.float32)
     B, n_q, H, d = qq.shape
     Nkv = KK.shape[1]
+    H_kv = 1 if KK.ndim == 3 else KK.shape[2]
+    assert H % H_kv == 0
     ii = None if idx is None else _np(idx, np.int32)
     k = 0 if ii is None else ii.shape[-1]
     rr = None if rows is None else _np(rows, np.int64)
     R = B * n_q if rr is None else rr.size
     out = np.empty((R, H, d), np.float64)
     lse = np.empty((R, H), np.float64)
-    lib().orc_attention(B, n_q, H, d, Nkv, _ptr(qq), _ptr(KK), _ptr(VV), float(tau),
+    lib().orc_attention(B, n_q, H, H_kv, d, Nkv, _ptr(qq), _ptr(KK), _ptr(VV), float(tau),
                         mode, q_pos0, m, window, _ptr(ii), k,
                         0 if rr is None else rr.size, _ptr(rr), _ptr(out), _ptr(lse))
     return out, lse
@@ -233,7 +251,7 @@ def _values(x, scale=None, kind="float"):
 
 
 def csa_index_topk(idx_q, idx_q_scale, q_kind, idx_k, idx_k_scale, k_kind,
-                   q_pos0: int, m: int, k: int, rows=None):
+                   q_pos0: int, m: int, k: int, rows=None, head_w=None, relu: bool = False):
     """Scores and selection for CSA: returns (fp64 scores, fp32 scores,
     top-k [R, k]).  k_kind "e2m1" takes packed codes + E4M3 block scales and
     runs the FP4 -> E4M3 conversion first."""
@@ -249,7 +267,7 @@ def csa_index_topk(idx_q, idx_q_scale, q_kind, idx_k, idx_k_scale, k_kind,
     if rows is None:
         qv = e4m3_decode(idx_q) if q_kind == "e4m3" else _np(idx_q, np.float32)
         qs = None if idx_q_scale is None else _np(idx_q_scale, np.float32)
-        s64, s32 = index_scores(qv, qs, kv, ks, q_pos0, m)
+        s64, s32 = index_scores(qv, qs, kv, ks, q_pos0, m, head_w=head_w, relu=relu)
         flat = np.arange(B * n_q)
     else:
         # only the requested rows' queries are decoded: each row is scored as
@@ -263,7 +281,9 @@ def csa_index_topk(idx_q, idx_q_scale, q_kind, idx_k, idx_k_scale, k_kind,
             qv = e4m3_decode(q1) if q_kind == "e4m3" else _np(q1, np.float32)
             qs = None if idx_q_scale is None else _np(idx_q_scale[b:b + 1, i:i + 1], np.float32)
             ks1 = None if ks is None else ks[b:b + 1]
-            s64[r:r + 1], s32[r:r + 1] = index_scores(qv, qs, kv[b:b + 1], ks1, q_pos0 + i, m)
+            hw1 = None if head_w is None else _np(head_w[b:b + 1, i:i + 1], np.float32)
+            s64[r:r + 1], s32[r:r + 1] = index_scores(qv, qs, kv[b:b + 1], ks1, q_pos0 + i, m, head_w=hw1,
+                                                      relu=relu)
     lens = visible(q_pos0 + flat % n_q, m, Nc)
     sel = topk(s32, lens, k)
     return s64, s32, sel

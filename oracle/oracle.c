@@ -156,6 +156,32 @@ ORC_API void orc_compress(int B, int n, int m, int d, const float* logits,
         }
 }
 
+/* a1 variant: per-channel compression weights -- a reading of "weighted
+ * aggregation" (加权聚合, "DeepSeek V4 技术解读" §2.1) in which every channel
+ * c carries its own logit per token: out[j][c] = sum_i w_{j,i,c} x[jm+i][c],
+ * w_{j,.,c} = softmax over the block of logits[jm+i][c].  logits: [B, n, d]. */
+ORC_API void orc_compress_per_channel(int B, int n, int m, int d, const float* logits,
+                                      const float* x, double* out)
+{
+    int Nc = n / m;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < Nc; ++j)
+            for (int c = 0; c < d; ++c) {
+                const float* lg = logits + ((int64_t)b * n + (int64_t)j * m) * d + c;
+                double mx = -INFINITY;
+                for (int i = 0; i < m; ++i) if (lg[(int64_t)i * d] > mx) mx = lg[(int64_t)i * d];
+                double den = 0.0;
+                for (int i = 0; i < m; ++i) den += exp((double)lg[(int64_t)i * d] - mx);
+                double acc = 0.0;
+                for (int i = 0; i < m; ++i) {
+                    double w = exp((double)lg[(int64_t)i * d] - mx) / den;
+                    acc += w * (double)x[((int64_t)b * n + (int64_t)j * m + i) * d + c];
+                }
+                out[((int64_t)b * Nc + j) * d + c] = acc;
+            }
+}
+
 /* Per-row E4M3 quantisation of compressed indexer keys (the compression
  * epilogue).  scale = amax / 448, code = E4M3(x * (448 / amax)), all in fp32;
  * a row with amax = 0 gets scale 1 and zero codes. */
@@ -256,12 +282,17 @@ static int64_t n_visible(int64_t t, int m, int64_t Nc)
  * s(t, j) = sum_h sq(t,h) * sk(j) * <q(t,h), k(j)>, heads summed in order
  * h = 0..H_I-1, for j < nv(t).  q and k hold the decoded stored values; the
  * scale arrays may be NULL (scale 1).  Entries j >= nv(t) are set to NaN.
+ * Variant reading of the page's "similarity" (§8 f3): with relu, each head's
+ * term uses max(<q, k>, 0) (the scales are positive, so this is the ReLU of
+ * the scaled dot product), and with head_w ([B, n_q, H_I]) each head's term
+ * is multiplied by w(t, h): s = sum_h w(t,h) * sq * sk * ReLU(<q, k>).
  * rows: NULL for all B*n_q rows, else n_rows flat indices b*n_q + i.
  * out64 gets the fp64 score, out32 (optional) the same value rounded to fp32,
  * the value the ranking uses. */
 ORC_API void orc_index_scores(int B, int n_q, int64_t q_pos0, int m, int Nc,
                               int HI, int dI, const float* q, const float* q_scale,
                               const float* k, const float* k_scale,
+                              const float* head_w, int relu,
                               int n_rows, const int64_t* rows,
                               double* out64, float* out32)
 {
@@ -283,7 +314,10 @@ ORC_API void orc_index_scores(int B, int n_q, int64_t q_pos0, int m, int Nc,
                     for (int c = 0; c < dI; ++c)
                         dot += (double)qt[h * dI + c] * (double)kr[c];
                     double sq = q_scale ? (double)q_scale[flat * HI + h] : 1.0;
-                    s += sq * sk * dot;
+                    if (relu && dot < 0.0) dot = 0.0;
+                    double term = sq * sk * dot;
+                    if (head_w) term *= (double)head_w[flat * HI + h];
+                    s += term;
                 }
             }
             if (out64) out64[r * Nc + j] = s;
@@ -342,9 +376,11 @@ ORC_API void orc_topk(int n_rows, const int64_t* lens, int64_t row_stride, int k
  *           entries < 0 are padding.
  *   mode 1, closed blocks (HCA, §2.2): j < nv(t) = min(floor((t+1)/m), N_kv).
  *   mode 2, window (§2.3): max(0, t-W+1) <= j <= min(t, N_kv-1).
- * q: [B, n_q, H, d]; K, V: [B, N_kv, d]; idx: [B, n_q, k].
+ * q: [B, n_q, H, d]; K, V: [B, N_kv, H_kv, d] (H_kv KV heads; query head h
+ * reads KV head h / (H / H_kv) -- H_kv = 1 is the shared head of the MLA
+ * reading, H_kv > 1 the GQA / MHA variant readings); idx: [B, n_q, k].
  * out: [R, H, d], lse: [R, H] for the R selected rows. */
-ORC_API void orc_attention(int B, int n_q, int H, int d, int64_t Nkv,
+ORC_API void orc_attention(int B, int n_q, int H, int H_kv, int d, int64_t Nkv,
                            const float* q, const float* K, const float* V,
                            double tau, int mode, int64_t q_pos0, int m,
                            int64_t window, const int32_t* idx, int k,
@@ -366,6 +402,7 @@ ORC_API void orc_attention(int B, int n_q, int H, int d, int64_t Nkv,
                 int64_t hi = t < Nkv - 1 ? t : Nkv - 1;
                 cnt = hi >= lo ? hi - lo + 1 : 0;
             }
+            const int64_t hk = h / (H / H_kv);    /* this head's KV head */
             const float* qh = q + (flat * H + h) * d;
             double* o = out + (r * H + h) * d;
             for (int c = 0; c < d; ++c) o[c] = 0.0;
@@ -374,7 +411,7 @@ ORC_API void orc_attention(int B, int n_q, int H, int d, int64_t Nkv,
                 int64_t j = sel ? sel[e] : lo + e;
                 if (j < 0) continue;
                 if (j >= Nkv) { mx = NAN; break; }
-                const float* kr = K + (b * Nkv + j) * d;
+                const float* kr = K + ((b * Nkv + j) * H_kv + hk) * d;
                 double s = 0.0;
                 for (int c = 0; c < d; ++c) s += (double)qh[c] * (double)kr[c];
                 s *= tau;
@@ -390,8 +427,8 @@ ORC_API void orc_attention(int B, int n_q, int H, int d, int64_t Nkv,
             for (int64_t e = 0; e < cnt; ++e) {
                 int64_t j = sel ? sel[e] : lo + e;
                 if (j < 0) continue;
-                const float* kr = K + (b * Nkv + j) * d;
-                const float* vr = V + (b * Nkv + j) * d;
+                const float* kr = K + ((b * Nkv + j) * H_kv + hk) * d;
+                const float* vr = V + ((b * Nkv + j) * H_kv + hk) * d;
                 double s = 0.0;
                 for (int c = 0; c < d; ++c) s += (double)qh[c] * (double)kr[c];
                 double p = exp(s * tau - mx);
