@@ -27,7 +27,8 @@
  *     head dim, H_I / d_I indexer heads and head dim, k top-k.  The query at
  *     absolute position t sees entry j iff (j + 1) * m - 1 <= t, i.e. the
  *     nv(t) = min(floor((t + 1) / m), N_c) first entries.
- *   - Attention uses one KV head shared by all H query heads.
+ *   - Attention uses one KV head shared by all H query heads (H_kv = 1); the
+ *     attention calls also take H_kv > 1 KV heads (GQA / MHA readings).
  */
 #ifndef CSA_H
 #define CSA_H
@@ -90,6 +91,19 @@ csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_stream
                           void* const* out_scale, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * csa_compress_per_channel -- the per-channel variant reading of "weighted
+ * aggregation" ("DeepSeek V4 技术解读" §2.1 KV Cache 压缩): every channel has
+ * its own logit per token, and
+ *     out[b, j, c] = sum_{i<m} softmax_i(logits[s][b, j*m + i, c]) x[b, j*m + i, c].
+ *   logits   host array of n_streams device pointers, fp32 [B, n, dim[s]].
+ *   Other arguments, outputs and requirements as in csa_compress.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_compress_per_channel(int B, int n, int m, int n_streams, const float* const* logits,
+                                      const void* const* x, const csa_dtype_t* x_dtype, const int* dim,
+                                      void* const* out, const csa_dtype_t* out_dtype,
+                                      void* const* out_scale, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * csa_index_scores -- Lightning Indexer scores ("DeepSeek V4 技术解读" §2.1,
  * 64 indexer heads x 128; §五 for the FP4 keys):
  *     s[b, i, j] = sum_h sq[b,i,h] * sk[b,j] * < q[b,i,h,:], k[b,j,:] >
@@ -106,6 +120,11 @@ csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_stream
  *            fp32 score rounded to nearest even; the score storage precision
  *            of "DeepSeek-V4 点评总结", FP4 量化感知训练: half the score
  *            traffic, at a recall cost the tests measure).
+ *   head_weight, relu  the weighted / ReLU variant reading of the indexer's
+ *            "similarity" (§2.1): head_weight device fp32 [B, n_q, H_I] (or
+ *            NULL: weight 1) and relu != 0 give
+ *            s = sk * sum_h w(t,h) * sq(t,h) * max(<q(t,h), k(j)>, 0).
+ *            NULL and 0 give the plain score above.
  * Precision pairs: (F32, F32) on CUDA cores; (BF16, BF16) and
  * (E4M3, E4M3 | E2M1) on tcgen05 tensor cores with fp32 accumulation, which
  * require H_I = 64 and d_I = 128.
@@ -114,6 +133,7 @@ size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dt
 csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
                               const void* q_idx, csa_dtype_t q_dtype, const float* q_scale,
                               const void* k_idx, csa_dtype_t k_dtype, const void* k_scale,
+                              const float* head_weight, int relu,
                               void* scores, csa_dtype_t score_dtype, void* workspace,
                               size_t workspace_bytes, csa_stream_t stream);
 
@@ -177,6 +197,7 @@ size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, 
 csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
                             int k, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale,
                             const void* k_idx, csa_dtype_t k_dtype, const void* k_scale,
+                            const float* head_weight, int relu,
                             csa_dtype_t score_dtype, int32_t* topk, void* workspace,
                             size_t workspace_bytes, csa_stream_t stream);
 
@@ -186,19 +207,24 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
  *     o[b,i,h,:] = sum_{j in topk[b,i,:], j >= 0} softmax_j(scale * <q, k_c[b,j]>) v_c[b,j,:]
  *     lse[b,i,h] = log sum_j exp(scale * <q, k_c[b,j]>)      (natural log)
  * An empty selection gives o = 0 and lse = -inf.
- *   q      device [B, n_q, H, d];  k_c, v_c  device [B, N_c, d];  all in dtype
- *          (CSA_F32 or CSA_BF16);  out  device [B, n_q, H, d] in dtype;
+ *   q      device [B, n_q, H, d];  k_c, v_c  device [B, N_c, H_kv, d];  all
+ *          in dtype (CSA_F32 or CSA_BF16);  out  device [B, n_q, H, d] in dtype;
+ *   H_kv   KV heads: 1 is the shared head of the MLA reading (the spec's);
+ *          H_kv > 1 (dividing H, H / H_kv a power of two <= 128) are the GQA
+ *          and MHA variant readings, query head h reading KV head
+ *          h / (H / H_kv);
  *   topk   device int32 [B, n_q, k], entries in [0, N_c) or -1;
  *   lse    device fp32 [B, n_q, H] or NULL.
- * Requirements: d in {64, 128}, H in {8, 16, 32, 64, 128}, scale > 0 and
- * finite (else CSA_ERR_INVALID_ARG).  Indices outside [-1, N_c) are skipped
- * and flagged in the device status word.
- * Precision: BF16 with d = 128 and H in {64, 128} runs on the tcgen05 tensor
- * cores (the probabilities enter the P.V product rounded to bf16, fp32
- * accumulation); other shapes and fp32 I/O run on CUDA cores in fp32.
+ * Requirements: d in {64, 128}, H in {8, 16, 32, 64, 128} for H_kv = 1,
+ * scale > 0 and finite (else CSA_ERR_INVALID_ARG).  Indices outside
+ * [-1, N_c) are skipped and flagged in the device status word.
+ * Precision: BF16 with one KV head, d = 128 and H in {64, 128} runs on the
+ * tcgen05 tensor cores (the probabilities enter the P.V product rounded to
+ * bf16, fp32 accumulation); other shapes, H_kv > 1 and fp32 I/O run on CUDA
+ * cores in fp32.
  * ------------------------------------------------------------------------- */
 size_t csa_sparse_attn_workspace_size(int B, int n_q, int H, int d, int k);
-csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float scale,
+csa_status_t csa_sparse_attn(int B, int n_q, int H, int H_kv, int d, int N_c, int k, float scale,
                              const void* q, const void* k_c, const void* v_c, csa_dtype_t dtype,
                              const int32_t* topk, void* out, float* lse,
                              void* workspace, size_t workspace_bytes, csa_stream_t stream);
@@ -209,16 +235,17 @@ csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float
  * j < nv(q_pos0 + i), with no selection.  Layouts and output as in
  * csa_sparse_attn.
  * ------------------------------------------------------------------------- */
-csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int d, float scale,
+csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int H_kv, int d, float scale,
                       const void* q, const void* k_c, const void* v_c, csa_dtype_t dtype,
                       void* out, float* lse, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * swa_attn -- sliding-window attention over raw tokens ("DeepSeek V4 技术解读"
  * §2.3): query i at t = q_pos0 + i sees tokens s with t - window < s <= t and
- * s < n_kv.  k, v device [B, n_kv, d]; other layouts as in csa_sparse_attn.
+ * s < n_kv.  k, v device [B, n_kv, H_kv, d]; other layouts as in
+ * csa_sparse_attn.
  * ------------------------------------------------------------------------- */
-csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int H, int d,
+csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int H, int H_kv, int d,
                       float scale, const void* q, const void* k, const void* v,
                       csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream);
 

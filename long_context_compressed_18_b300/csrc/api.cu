@@ -135,11 +135,11 @@ SplitPlan attn_split_plan(int n_q, long long set_len)
 // maxima there (the top-k's collection threshold).
 csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos0, int m, int N_c, int H_I,
                         int d_I, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
-                        csa_dtype_t k_dtype, const void* k_scale, void* scores, bool sbf16, void* ws, cudaStream_t s,
-                        uint32_t* wmax = nullptr, int wmax_ld = 0)
+                        csa_dtype_t k_dtype, const void* k_scale, const float* head_w, bool relu, void* scores,
+                        bool sbf16, void* ws, cudaStream_t s, uint32_t* wmax = nullptr, int wmax_ld = 0)
 {
     if (q_dtype == CSA_F32) {
-        return cuda_status(launch_indexer_f32(reinterpret_cast<const float*>(q_idx), q_scale,
+        return cuda_status(launch_indexer_f32(reinterpret_cast<const float*>(q_idx), q_scale, head_w, relu,
                                               reinterpret_cast<const float*>(k_idx),
                                               reinterpret_cast<const float*>(k_scale), scores, sbf16, B, n_q, i_start,
                                               n_q_rows, q_pos0, m, N_c, H_I, d_I, s),
@@ -169,7 +169,8 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos
     if (st != CSA_OK) return st;
     st = make_map(&tk, keys, dt, (uint64_t)d_I, (uint64_t)B * N_c, (uint64_t)d_I * elem, box_inner, 128);
     if (st != CSA_OK) return st;
-    return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, ksc, scores, sbf16, B, n_q, i_start, n_q_rows,
+    return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, head_w, relu, ksc, scores, sbf16, B, n_q, i_start,
+                                         n_q_rows,
                                          q_pos0, m, N_c, num_sms(), wmax, wmax_ld, s),
                        "indexer_tc launch");
 }
@@ -223,13 +224,18 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns, unsigned* stopped_by_abo
 // ---------------------------------------------------------------------------
 // attention
 // ---------------------------------------------------------------------------
-static csa_status_t check_attn(int B, int n_q, int H, int d, long long N_kv, float scale, const void* q, const void* k,
-                               const void* v, csa_dtype_t dtype, const void* out, const float* lse)
+static csa_status_t check_attn(int B, int n_q, int H, int H_kv, int d, long long N_kv, float scale, const void* q,
+                               const void* k, const void* v, csa_dtype_t dtype, const void* out, const float* lse)
 {
     if (B < 0 || n_q < 0 || N_kv < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes");
     if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CSA_ERR_INVALID_ARG, "scale must be positive and finite");
     if (dtype != CSA_F32 && dtype != CSA_BF16) return fail(CSA_ERR_UNSUPPORTED, "attention dtype must be F32 or BF16");
-    if (!attn_simt_supported(H, d)) return fail(CSA_ERR_UNSUPPORTED, "attention needs H in {8,16,32,64,128}, d in {64,128}");
+    if (H_kv < 1 || H < H_kv || H % H_kv) return fail(CSA_ERR_INVALID_ARG, "H_kv must divide H (H=%d, H_kv=%d)", H, H_kv);
+    if (H_kv == 1 && !attn_simt_supported(H, d))
+        return fail(CSA_ERR_UNSUPPORTED, "attention needs H in {8,16,32,64,128}, d in {64,128}");
+    const int G = H / H_kv;
+    if (H_kv > 1 && ((G & (G - 1)) || G > 128 || (d != 64 && d != 128)))
+        return fail(CSA_ERR_UNSUPPORTED, "attention needs H / H_kv a power of two <= 128 and d in {64,128}");
     if ((long long)B * n_q == 0) return CSA_OK;
     if (!q || !out || (N_kv > 0 && (!k || !v))) return fail(CSA_ERR_INVALID_ARG, "NULL tensor");
     if (!aligned16(q) || !aligned16(out) || (k && !aligned16(k)) || (v && !aligned16(v)) || (lse && !aligned16(lse)))
@@ -278,12 +284,13 @@ static csa_status_t run_attn_tc(int mode, int B, int n_q, int64_t q_pos0, int m,
 
 template <typename TIO>
 static csa_status_t run_attn(int mode, int B, int n_q, int64_t q_pos0, int m, long long window, long long N_kv, int H,
-                             int d, int k, float scale, const void* q, const void* kp, const void* vp, const int32_t* topk,
-                             void* out, float* lse, SplitPlan sp, void* ws, cudaStream_t s)
+                             int H_kv, int d, int k, float scale, const void* q, const void* kp, const void* vp,
+                             const int32_t* topk, void* out, float* lse, SplitPlan sp, void* ws, cudaStream_t s)
 {
     if constexpr (std::is_same<TIO, __nv_bfloat16>::value) {
-        // the tensor-core kernel stages at most 4096 selected entries per CTA
-        if (attn_tc_supported(H, d) && N_kv > 0 && (mode != 0 || k <= 4096)) {
+        // the tensor-core kernel (one shared KV head) stages at most 4096
+        // selected entries per CTA
+        if (H_kv == 1 && attn_tc_supported(H, d) && N_kv > 0 && (mode != 0 || k <= 4096)) {
             // TMA row coordinates are 32-bit
             if ((long long)B * n_q * H + 128 > INT32_MAX || (long long)B * N_kv + 128 > INT32_MAX)
                 return fail(CSA_ERR_UNSUPPORTED, "attention tensors exceed 2^31 rows");
@@ -308,11 +315,14 @@ static csa_status_t run_attn(int mode, int B, int n_q, int64_t q_pos0, int m, lo
     a.k = k;
     a.m = m;
     a.n_splits = sp.n;
+    a.H_kv = H_kv;
+    a.H_tot = H;
+    a.G = H / H_kv;
     if (sp.n > 1) {
         a.part_o = reinterpret_cast<float*>(ws);
         a.part_ml = a.part_o + (size_t)sp.n * B * n_q * H * d;
     }
-    return cuda_status(launch_attn_simt<TIO>(a, H, d, s), "attention launch");
+    return cuda_status(launch_attn_simt<TIO>(a, H / H_kv, d, s), "attention launch");
 }
 
 static size_t sparse_ws(int B, int n_q, int H, int d, int k)
@@ -324,8 +334,9 @@ static size_t sparse_ws(int B, int n_q, int H, int d, int k)
 
 static csa_status_t check_index_args(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I,
                                      const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
-                                     csa_dtype_t k_dtype, const void* k_scale)
+                                     csa_dtype_t k_dtype, const void* k_scale, const float* head_w = nullptr)
 {
+    if (head_w && !aligned16(head_w)) return fail(CSA_ERR_ALIGNMENT, "head_weight not 16-byte aligned");
     if (B < 0 || n_q < 0 || m < 1 || N_c < 0 || H_I < 1 || d_I < 1 || q_pos0 < 0)
         return fail(CSA_ERR_INVALID_ARG, "bad sizes");
     csa_status_t st = check_index_dtypes(q_dtype, k_dtype, H_I, d_I);
@@ -384,17 +395,11 @@ csa_status_t csa_device_status(csa_stream_t stream)
     return CSA_OK;
 }
 
-csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_streams, const void* const* x,
-                          const csa_dtype_t* x_dtype, const int* dim, void* const* out, const csa_dtype_t* out_dtype,
-                          void* const* out_scale, csa_stream_t stream)
+// Argument checks shared by the compression entry points.
+static csa_status_t check_compress_streams(int n_streams, const void* const* x, const csa_dtype_t* x_dtype,
+                                           const int* dim, void* const* out, const csa_dtype_t* out_dtype,
+                                           void* const* out_scale)
 {
-    if (B < 0 || n < 0 || m < 1) return fail(CSA_ERR_INVALID_ARG, "bad sizes B=%d n=%d m=%d", B, n, m);
-    if (n_streams < 1 || n_streams > 4 || !x || !x_dtype || !dim || !out || !out_dtype)
-        return fail(CSA_ERR_INVALID_ARG, "bad stream arrays (n_streams=%d)", n_streams);
-    const int Nc = n / m;
-    if ((long long)B * Nc == 0) return CSA_OK;
-    if (!logits) return fail(CSA_ERR_INVALID_ARG, "logits is NULL");
-    if (!aligned16(logits)) return fail(CSA_ERR_ALIGNMENT, "logits not 16-byte aligned");
     for (int s = 0; s < n_streams; ++s) {
         const int d = dim[s];
         const bool pow2 = d >= 8 && d <= 256 && (d & (d - 1)) == 0;
@@ -412,11 +417,29 @@ csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_stream
             return fail(CSA_ERR_INVALID_ARG, "stream %d: bad output dtype", s);
         }
     }
+    return CSA_OK;
+}
+
+static int out_kind_of(csa_dtype_t od) { return od == CSA_F32 ? 0 : od == CSA_BF16 ? 1 : od == CSA_E4M3 ? 2 : 3; }
+
+csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_streams, const void* const* x,
+                          const csa_dtype_t* x_dtype, const int* dim, void* const* out, const csa_dtype_t* out_dtype,
+                          void* const* out_scale, csa_stream_t stream)
+{
+    if (B < 0 || n < 0 || m < 1) return fail(CSA_ERR_INVALID_ARG, "bad sizes B=%d n=%d m=%d", B, n, m);
+    if (n_streams < 1 || n_streams > 4 || !x || !x_dtype || !dim || !out || !out_dtype)
+        return fail(CSA_ERR_INVALID_ARG, "bad stream arrays (n_streams=%d)", n_streams);
+    const int Nc = n / m;
+    if ((long long)B * Nc == 0) return CSA_OK;
+    if (!logits) return fail(CSA_ERR_INVALID_ARG, "logits is NULL");
+    if (!aligned16(logits)) return fail(CSA_ERR_ALIGNMENT, "logits not 16-byte aligned");
+    csa_status_t cst = check_compress_streams(n_streams, x, x_dtype, dim, out, out_dtype, out_scale);
+    if (cst != CSA_OK) return cst;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int kinds[4];
     bool bf16_in[4];
     for (int s = 0; s < n_streams; ++s) {
-        kinds[s] = out_dtype[s] == CSA_F32 ? 0 : out_dtype[s] == CSA_BF16 ? 1 : out_dtype[s] == CSA_E4M3 ? 2 : 3;
+        kinds[s] = out_kind_of(out_dtype[s]);
         bf16_in[s] = x_dtype[s] == CSA_BF16;
     }
     if (compress_tiles_supported(n, m, n_streams, dim, bf16_in)) {
@@ -433,6 +456,30 @@ csa_status_t csa_compress(int B, int n, int m, const float* logits, int n_stream
     return CSA_OK;
 }
 
+csa_status_t csa_compress_per_channel(int B, int n, int m, int n_streams, const float* const* logits,
+                                      const void* const* x, const csa_dtype_t* x_dtype, const int* dim,
+                                      void* const* out, const csa_dtype_t* out_dtype, void* const* out_scale,
+                                      csa_stream_t stream)
+{
+    if (B < 0 || n < 0 || m < 1) return fail(CSA_ERR_INVALID_ARG, "bad sizes B=%d n=%d m=%d", B, n, m);
+    if (n_streams < 1 || n_streams > 4 || !logits || !x || !x_dtype || !dim || !out || !out_dtype)
+        return fail(CSA_ERR_INVALID_ARG, "bad stream arrays (n_streams=%d)", n_streams);
+    if ((long long)B * (n / m) == 0) return CSA_OK;
+    for (int s = 0; s < n_streams; ++s) {
+        if (!logits[s]) return fail(CSA_ERR_INVALID_ARG, "stream %d: logits NULL", s);
+        if (!aligned16(logits[s])) return fail(CSA_ERR_ALIGNMENT, "stream %d: logits not 16-byte aligned", s);
+    }
+    csa_status_t cst = check_compress_streams(n_streams, x, x_dtype, dim, out, out_dtype, out_scale);
+    if (cst != CSA_OK) return cst;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    for (int s = 0; s < n_streams; ++s) {
+        cudaError_t e = launch_compress_per_channel(B, n, m, dim[s], logits[s], x[s], x_dtype[s] == CSA_BF16, out[s],
+                                                    out_kind_of(out_dtype[s]), out_scale ? out_scale[s] : nullptr, st);
+        if (e != cudaSuccess) return cuda_status(e, "compress (per channel) launch");
+    }
+    return CSA_OK;
+}
+
 size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dtype)
 {
     if (B < 0 || N_c < 0 || d_I < 0) return 0;
@@ -442,10 +489,11 @@ size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dt
 
 csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, const void* q_idx,
                               csa_dtype_t q_dtype, const float* q_scale, const void* k_idx, csa_dtype_t k_dtype,
-                              const void* k_scale, void* scores, csa_dtype_t score_dtype, void* workspace,
-                              size_t workspace_bytes, csa_stream_t stream)
+                              const void* k_scale, const float* head_weight, int relu, void* scores,
+                              csa_dtype_t score_dtype, void* workspace, size_t workspace_bytes, csa_stream_t stream)
 {
-    csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale);
+    csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+                                       head_weight);
     if (st != CSA_OK) return st;
     st = check_score_dtype(score_dtype);
     if (st != CSA_OK) return st;
@@ -455,7 +503,8 @@ csa_status_t csa_index_scores(int B, int n_q, int64_t q_pos0, int m, int N_c, in
     if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     return run_scores(B, n_q, 0, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                      scores, score_dtype == CSA_BF16, workspace, reinterpret_cast<cudaStream_t>(stream));
+                      head_weight, relu != 0, scores, score_dtype == CSA_BF16, workspace,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t csa_topk_select_workspace_size(int B, int n_q, int N_c, int k)
@@ -500,10 +549,12 @@ size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, 
 
 csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
                             const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
-                            csa_dtype_t k_dtype, const void* k_scale, csa_dtype_t score_dtype, int32_t* topk,
-                            void* workspace, size_t workspace_bytes, csa_stream_t stream)
+                            csa_dtype_t k_dtype, const void* k_scale, const float* head_weight, int relu,
+                            csa_dtype_t score_dtype, int32_t* topk, void* workspace, size_t workspace_bytes,
+                            csa_stream_t stream)
 {
-    csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale);
+    csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+                                       head_weight);
     if (st != CSA_OK) return st;
     st = check_topk(N_c, k);
     if (st != CSA_OK) return st;
@@ -532,7 +583,7 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
             // with its collection threshold taken from them
             const int ld = topk_wmax_ld(N_c);
             st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                            scores, sbf16, w_scores_ws, s, w_wmax, ld);
+                            head_weight, relu != 0, scores, sbf16, w_scores_ws, s, w_wmax, ld);
             if (st != CSA_OK) return st;
             st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q,
                                          w_topk, s, w_wmax, ld),
@@ -542,7 +593,7 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
         }
         if (N_c > 0) {
             st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                            scores, sbf16, w_scores_ws, s);
+                            head_weight, relu != 0, scores, sbf16, w_scores_ws, s);
             if (st != CSA_OK) return st;
         }
         st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk, s),
@@ -558,11 +609,11 @@ size_t csa_sparse_attn_workspace_size(int B, int n_q, int H, int d, int k)
     return sparse_ws(B, n_q, H, d, k);
 }
 
-csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float scale, const void* q, const void* k_c,
-                             const void* v_c, csa_dtype_t dtype, const int32_t* topk, void* out, float* lse,
-                             void* workspace, size_t workspace_bytes, csa_stream_t stream)
+csa_status_t csa_sparse_attn(int B, int n_q, int H, int H_kv, int d, int N_c, int k, float scale, const void* q,
+                             const void* k_c, const void* v_c, csa_dtype_t dtype, const int32_t* topk, void* out,
+                             float* lse, void* workspace, size_t workspace_bytes, csa_stream_t stream)
 {
-    csa_status_t st = check_attn(B, n_q, H, d, N_c, scale, q, k_c, v_c, dtype, out, lse);
+    csa_status_t st = check_attn(B, n_q, H, H_kv, d, N_c, scale, q, k_c, v_c, dtype, out, lse);
     if (st != CSA_OK) return st;
     if (k < 1) return fail(CSA_ERR_INVALID_ARG, "k must be >= 1");
     if ((long long)B * n_q == 0) return CSA_OK;
@@ -573,34 +624,42 @@ csa_status_t csa_sparse_attn(int B, int n_q, int H, int d, int N_c, int k, float
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == CSA_BF16)
-        return run_attn<__nv_bfloat16>(0, B, n_q, 0, 1, 0, N_c, H, d, k, scale, q, k_c, v_c, topk, out, lse, splits, workspace, s);
-    return run_attn<float>(0, B, n_q, 0, 1, 0, N_c, H, d, k, scale, q, k_c, v_c, topk, out, lse, splits, workspace, s);
+        return run_attn<__nv_bfloat16>(0, B, n_q, 0, 1, 0, N_c, H, H_kv, d, k, scale, q, k_c, v_c, topk, out, lse, splits,
+                                       workspace, s);
+    return run_attn<float>(0, B, n_q, 0, 1, 0, N_c, H, H_kv, d, k, scale, q, k_c, v_c, topk, out, lse, splits, workspace,
+                           s);
 }
 
-csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int d, float scale, const void* q,
-                      const void* k_c, const void* v_c, csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream)
+csa_status_t hca_attn(int B, int n_q, int64_t q_pos0, int m, int N_c, int H, int H_kv, int d, float scale,
+                      const void* q, const void* k_c, const void* v_c, csa_dtype_t dtype, void* out, float* lse,
+                      csa_stream_t stream)
 {
     if (m < 1 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad m / q_pos0");
-    csa_status_t st = check_attn(B, n_q, H, d, N_c, scale, q, k_c, v_c, dtype, out, lse);
+    csa_status_t st = check_attn(B, n_q, H, H_kv, d, N_c, scale, q, k_c, v_c, dtype, out, lse);
     if (st != CSA_OK) return st;
     if ((long long)B * n_q == 0) return CSA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == CSA_BF16)
-        return run_attn<__nv_bfloat16>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
-    return run_attn<float>(1, B, n_q, q_pos0, m, 0, N_c, H, d, 0, scale, q, k_c, v_c, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
+        return run_attn<__nv_bfloat16>(1, B, n_q, q_pos0, m, 0, N_c, H, H_kv, d, 0, scale, q, k_c, v_c, nullptr, out,
+                                       lse, SplitPlan{1, 1 << 30}, nullptr, s);
+    return run_attn<float>(1, B, n_q, q_pos0, m, 0, N_c, H, H_kv, d, 0, scale, q, k_c, v_c, nullptr, out, lse,
+                           SplitPlan{1, 1 << 30}, nullptr, s);
 }
 
-csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int H, int d, float scale, const void* q,
-                      const void* k, const void* v, csa_dtype_t dtype, void* out, float* lse, csa_stream_t stream)
+csa_status_t swa_attn(int B, int n_q, int64_t q_pos0, int n_kv, int window, int H, int H_kv, int d, float scale,
+                      const void* q, const void* k, const void* v, csa_dtype_t dtype, void* out, float* lse,
+                      csa_stream_t stream)
 {
     if (window < 1 || q_pos0 < 0) return fail(CSA_ERR_INVALID_ARG, "bad window / q_pos0");
-    csa_status_t st = check_attn(B, n_q, H, d, n_kv, scale, q, k, v, dtype, out, lse);
+    csa_status_t st = check_attn(B, n_q, H, H_kv, d, n_kv, scale, q, k, v, dtype, out, lse);
     if (st != CSA_OK) return st;
     if ((long long)B * n_q == 0) return CSA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == CSA_BF16)
-        return run_attn<__nv_bfloat16>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
-    return run_attn<float>(2, B, n_q, q_pos0, 1, window, n_kv, H, d, 0, scale, q, k, v, nullptr, out, lse, SplitPlan{1, 1 << 30}, nullptr, s);
+        return run_attn<__nv_bfloat16>(2, B, n_q, q_pos0, 1, window, n_kv, H, H_kv, d, 0, scale, q, k, v, nullptr, out,
+                                       lse, SplitPlan{1, 1 << 30}, nullptr, s);
+    return run_attn<float>(2, B, n_q, q_pos0, 1, window, n_kv, H, H_kv, d, 0, scale, q, k, v, nullptr, out, lse,
+                           SplitPlan{1, 1 << 30}, nullptr, s);
 }
 
 }  // extern "C"

@@ -1,10 +1,13 @@
-// Attention of H query heads over one shared KV head, for the three key sets
-// of the hybrid stack ("DeepSeek V4 技术解读"):
+// Attention of H query heads over one shared KV head (or, in the GQA / MHA
+// variant readings, over H_kv KV heads, query head h reading KV head
+// h / (H / H_kv)), for the three key sets of the hybrid stack ("DeepSeek V4
+// 技术解读"):
 //   mode 0  CSA core attention over the top-k selected entries (§2.1),
 //   mode 1  HCA dense attention over all closed compressed blocks (§2.2),
 //   mode 2  sliding-window attention over raw tokens (§2.3).
 //
-// CUDA-core kernel.  One CTA handles one query token (all heads) over one
+// CUDA-core kernel.  One CTA handles one query token and one KV head (the
+// query heads that share it; at least 8 rows, idle ones never stored) over one
 // contiguous slice of its key set; keys are staged in shared memory in tiles
 // of 32 (gathered by index for mode 0), scores and an online softmax (base-2,
 // fp32) run in registers, and P.V accumulates per thread over a slice of the
@@ -43,6 +46,10 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
     const int i = blockIdx.x / a.n_splits, split = blockIdx.x % a.n_splits;
     const long long row = (long long)b * a.n_q + i;
     const long long t = a.q_pos0 + i;
+    const int kvh = blockIdx.z;                    // this CTA's KV head
+    const int HT = a.H_tot;                        // query heads of a token
+    const int h0 = kvh * a.G;                      // its first query head
+    const bool h_live = h < a.G;                   // rows past G (when G < H) are idle
 
     // key-set slice [lo, hi) of this CTA: list positions (mode 0) or key indices
     long long set_lo, set_len;
@@ -57,12 +64,17 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
     const long long s_lo = set_lo + (long long)split * per;
     const long long s_hi = set_lo + min(set_len, (long long)(split + 1) * per);
 
-    // stage Q (pre-scaled to the base-2 domain)
-    const TIO* qp = a.q + row * H * D;
+    // stage Q (pre-scaled to the base-2 domain); idle rows are zero
+    const TIO* qp = a.q + (row * HT + h0) * D;
     for (int x = tid * 8; x < H * D; x += ATT_THREADS * 8) {
         float v[8];
-        Vec8<TIO>::load(qp + x, v);
         const int hh = x / D, c = x % D;
+        if (hh < a.G) {
+            Vec8<TIO>::load(qp + x, v);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = 0.f;
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) Qs[hh * QLD + c + u] = v[u] * a.scale_log2;
     }
@@ -96,7 +108,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
             const int e = x / (D / 8), c = (x % (D / 8)) * 8;
             float kv[8], vv[8];
             if (kvalid[e]) {
-                const long long off = ((long long)b * a.N_kv + kidx[e]) * D + c;
+                const long long off = (((long long)b * a.N_kv + kidx[e]) * a.H_kv + kvh) * D + c;
                 Vec8<TIO>::load(a.k_ptr + off, kv);
                 Vec8<TIO>::load(a.v_ptr + off, vv);
             } else {
@@ -158,7 +170,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
         float ov[CPT];
 #pragma unroll
         for (int u = 0; u < CPT; ++u) ov[u] = o[u] * inv;
-        TIO* op = a.out + (row * H + h) * D + tq * CPT;
+        TIO* op = a.out + (row * HT + h0 + h) * D + tq * CPT;
+        if (!h_live) return;
         if constexpr (CPT % 8 == 0) {
 #pragma unroll
             for (int u = 0; u < CPT; u += 8) {
@@ -175,9 +188,10 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
             }
         }
         if (a.lse && tq == 0)
-            a.lse[row * H + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            a.lse[row * HT + h0 + h] = l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     } else {
-        const long long prow = ((long long)split * a.B * a.n_q + row) * H + h;
+        if (!h_live) return;
+        const long long prow = ((long long)split * a.B * a.n_q + row) * HT + h0 + h;
         float* po = a.part_o + prow * D + tq * CPT;
 #pragma unroll
         for (int u = 0; u < CPT; ++u) po[u] = o[u];
@@ -264,12 +278,12 @@ static cudaError_t launch_h(const AttnArgsT<TIO>& a, cudaStream_t s)
     auto kern = attn_simt_kernel<TIO, H, D>;
     const size_t smem = attn_smem_bytes(H, D);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    dim3 grid(a.n_q * a.n_splits, a.B);
+    dim3 grid(a.n_q * a.n_splits, a.B, a.H_kv);
     kern<<<grid, ATT_THREADS, smem, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_splits == 1) return e;
-    const long long n = (long long)a.B * a.n_q * H * (D / 8);
-    attn_combine_kernel<TIO><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, H, D);
+    const long long n = (long long)a.B * a.n_q * a.H_tot * (D / 8);
+    attn_combine_kernel<TIO><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, a.H_tot, D);
     return cudaGetLastError();
 }
 
@@ -284,7 +298,8 @@ cudaError_t launch_attn_combine(const AttnArgsT<__nv_bfloat16>& a, int H, int D,
 template <typename TIO, int D>
 static cudaError_t launch_d(const AttnArgsT<TIO>& a, int H, cudaStream_t s)
 {
-    switch (H) {
+    // a CTA's rows: the G query heads of one KV head, at least 8
+    switch (H < 8 ? 8 : H) {
         case 8: return launch_h<TIO, 8, D>(a, s);
         case 16: return launch_h<TIO, 16, D>(a, s);
         case 32: return launch_h<TIO, 32, D>(a, s);
@@ -295,9 +310,15 @@ static cudaError_t launch_d(const AttnArgsT<TIO>& a, int H, cudaStream_t s)
 }
 
 template <typename TIO>
-cudaError_t launch_attn_simt(const AttnArgsT<TIO>& a, int H, int D, cudaStream_t s)
+cudaError_t launch_attn_simt(const AttnArgsT<TIO>& a_in, int H, int D, cudaStream_t s)
 {
-    if (a.B * a.n_q == 0) return cudaSuccess;
+    if (a_in.B * a_in.n_q == 0) return cudaSuccess;
+    AttnArgsT<TIO> a = a_in;
+    if (a.H_tot == 0) {   // one shared KV head
+        a.H_kv = 1;
+        a.H_tot = H;
+        a.G = H;
+    }
     if (D == 64) return launch_d<TIO, 64>(a, H, s);
     return launch_d<TIO, 128>(a, H, s);
 }

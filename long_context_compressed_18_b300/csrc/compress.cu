@@ -186,6 +186,88 @@ cudaError_t launch_compress(int B, int n, int m, int d, const float* logits, con
 }
 
 // ---------------------------------------------------------------------------
+// Per-channel compression weights (a variant reading of "weighted
+// aggregation", "DeepSeek V4 技术解读" §2.1): every channel c has its own
+// logit per token, logits [B, n, d], and
+//     out[b, j, c] = sum_i softmax_i(logits[b, jm + i, c]) x[b, jm + i, c].
+// One thread owns 8 consecutive channels of one entry: the block maxima, then
+// the exponentials' sum and the weighted sum in token order, then the
+// division -- fp32 throughout -- and the shared quantising epilogues.
+// ---------------------------------------------------------------------------
+template <typename Tin, int OUT>
+__global__ void __launch_bounds__(256, 4) compress_channel_kernel(int B, int n, int m, int Nc, int d,
+                                                               const float* __restrict__ logits,
+                                                               const Tin* __restrict__ x, void* out,
+                                                               void* out_scale)
+{
+    const int G = d >> 3;   // threads per output row (power of two, <= 32)
+    const long long rows = (long long)B * Nc;
+    const long long row = (long long)blockIdx.x * (256 / G) + threadIdx.x / G;
+    const int g = threadIdx.x & (G - 1);
+    const bool live = row < rows;
+    const long long r = live ? row : rows - 1;   // dead lanes mirror the last row
+    const long long b = r / Nc, j = r % Nc;
+    const long long base = (b * n + j * (long long)m) * d + 8 * g;
+    float mx[8], den[8], acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        mx[c] = -INFINITY;
+        den[c] = 0.f;
+        acc[c] = 0.f;
+    }
+    for (int i = 0; i < m; ++i) {
+        float l[8];
+        Vec8<float>::load(logits + base + (long long)i * d, l);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], l[c]);
+    }
+    for (int i = 0; i < m; ++i) {
+        float l[8], v[8];
+        Vec8<float>::load(logits + base + (long long)i * d, l);
+        Vec8<Tin>::load(x + base + (long long)i * d, v);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float e = expf(l[c] - mx[c]);
+            den[c] += e;
+            acc[c] = fmaf(e, v[c], acc[c]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = __fdiv_rn(acc[c], den[c]);
+    compress_store<OUT>(acc, g, G, r, d, out, out_scale, live);
+}
+
+cudaError_t launch_compress_per_channel(int B, int n, int m, int d, const float* logits, const void* x, bool x_bf16,
+                                        void* out, int out_kind, void* out_scale, cudaStream_t s)
+{
+    const int Nc = n / m;
+    const long long rows = (long long)B * Nc;
+    if (rows == 0) return cudaSuccess;
+    const int rows_per_cta = 256 / (d / 8);
+    const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
+#define CSA_LAUNCH_CHANNEL(TIN, OK)                                                                  \
+    compress_channel_kernel<TIN, OK><<<grid, 256, 0, s>>>(B, n, m, Nc, d, logits,                    \
+                                                          reinterpret_cast<const TIN*>(x), out, out_scale)
+    if (x_bf16) {
+        switch (out_kind) {
+            case 0: CSA_LAUNCH_CHANNEL(__nv_bfloat16, 0); break;
+            case 1: CSA_LAUNCH_CHANNEL(__nv_bfloat16, 1); break;
+            case 2: CSA_LAUNCH_CHANNEL(__nv_bfloat16, 2); break;
+            default: CSA_LAUNCH_CHANNEL(__nv_bfloat16, 3); break;
+        }
+    } else {
+        switch (out_kind) {
+            case 0: CSA_LAUNCH_CHANNEL(float, 0); break;
+            case 1: CSA_LAUNCH_CHANNEL(float, 1); break;
+            case 2: CSA_LAUNCH_CHANNEL(float, 2); break;
+            default: CSA_LAUNCH_CHANNEL(float, 3); break;
+        }
+    }
+#undef CSA_LAUNCH_CHANNEL
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Short blocks: tiles of R entries x every stream, streamed by bulk copies.
 // ---------------------------------------------------------------------------
 namespace cmpt {

@@ -62,11 +62,20 @@ template <bool FP8, int T> struct Cfg {
 // accumulator columns (lo = heads 0-31, hi = heads 32-63) with paired FMAs,
 // times the key scale; stored if key < nv (the token's visible entries; -1
 // for a token past the end of the rows) as fp32, or rounded to bf16 (nearest
-// even) when sbf16.  Returns the stored value.
-__device__ __forceinline__ float idx_store_score(const uint32_t (&lo)[32], const uint32_t (&hi)[32],
+// even) when sbf16.  RELU clips each head's accumulator at 0 first (sq[h]
+// then also carries the head's weight).  Returns the stored value.
+template <bool RELU>
+__device__ __forceinline__ float idx_store_score(uint32_t (&lo)[32], uint32_t (&hi)[32],
                                                  const float* __restrict__ sq, float sk, int key, int nv,
                                                  void* __restrict__ srow_ptr, bool sbf16)
 {
+    if constexpr (RELU) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            lo[h] = __float_as_uint(fmaxf(__uint_as_float(lo[h]), 0.f));
+            hi[h] = __float_as_uint(fmaxf(__uint_as_float(hi[h]), 0.f));
+        }
+    }
     const float4* sq4 = reinterpret_cast<const float4*>(sq);
     uint64_t pa = 0, pb = 0, pc = 0, pd = 0;   // packed partial sums (x, y halves)
 #pragma unroll
@@ -100,9 +109,9 @@ __device__ __forceinline__ float idx_store_score(const uint32_t (&lo)[32], const
 template <bool FP8, int T, bool WMAX>
 __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-    const float* __restrict__ q_scale, const float* __restrict__ k_scale, void* __restrict__ scores,
-    int score_bf16, int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int n_splits,
-    int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
+    const float* __restrict__ q_scale, const float* __restrict__ head_w, int relu, const float* __restrict__ k_scale,
+    void* __restrict__ scores, int score_bf16, int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m,
+    int Nc, int n_splits, int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
 {
     using C = idx::Cfg<FP8, T>;
     static_assert(!WMAX || T == 1, "warp maxima: decode groups");
@@ -225,7 +234,11 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             const int tt = x / idx::HEADS, h = x % idx::HEADS;
             const int i = i0 + tt;
             float v = 0.f;
-            if (i < n_q_rows) v = q_scale ? q_scale[((long long)b * n_q_total + i_start + i) * idx::HEADS + h] : 1.f;
+            if (i < n_q_rows) {
+                const long long qh = ((long long)b * n_q_total + i_start + i) * idx::HEADS + h;
+                v = q_scale ? q_scale[qh] : 1.f;
+                if (head_w) v *= head_w[qh];   // weighted variant: the head's weight joins its scale
+            }
             sq_s[x] = v;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
@@ -255,7 +268,8 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar_acc_empty[acc]);
-            const float sc = idx_store_score(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr, sbf16);
+            const float sc = relu ? idx_store_score<true>(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr, sbf16)
+                                  : idx_store_score<false>(va, vb, sq_s + tt0 * idx::HEADS, sk, key, nv_tok, srow_ptr, sbf16);
             if constexpr (WMAX) {
                 const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, key < nv_tok ? score_key(sc) : 0u);
                 const int grp = (tile0 + li) * (idx::BLOCK_KEYS / 32) + quad;   // keys 32 grp .. 32 grp + 31
@@ -277,17 +291,17 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
 // fp32 scores on CUDA cores (any H_I, d_I): one thread per (query, entry).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) indexer_f32_kernel(
-    const float* __restrict__ q, const float* __restrict__ q_scale, const float* __restrict__ k,
-    const float* __restrict__ k_scale, void* __restrict__ scores, int score_bf16, int n_q_total, int i_start,
-    int n_q_rows, long long q_pos0, int m, int Nc, int HI, int dI)
+    const float* __restrict__ q, const float* __restrict__ q_scale, const float* __restrict__ head_w, int relu,
+    const float* __restrict__ k, const float* __restrict__ k_scale, void* __restrict__ scores, int score_bf16,
+    int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int HI, int dI)
 {
     extern __shared__ float qs[];
     const int r = blockIdx.y;          // chunk-local row = b * n_q_rows + i
     const int b = r / n_q_rows, i = r % n_q_rows;
     const long long qrow = (long long)b * n_q_total + i_start + i;
     for (int x = threadIdx.x; x < HI * dI; x += blockDim.x) qs[x] = q[qrow * HI * dI + x];
-    if (q_scale)
-        for (int x = threadIdx.x; x < HI; x += blockDim.x) qs[HI * dI + x] = q_scale[qrow * HI + x];
+    for (int x = threadIdx.x; x < HI; x += blockDim.x)
+        qs[HI * dI + x] = (q_scale ? q_scale[qrow * HI + x] : 1.f) * (head_w ? head_w[qrow * HI + x] : 1.f);
     __syncthreads();
     long long nvl = (q_pos0 + i_start + i + 1) / m;
     const int nv = (int)(nvl < Nc ? nvl : Nc);
@@ -299,8 +313,8 @@ __global__ void __launch_bounds__(256) indexer_f32_kernel(
     for (int h = 0; h < HI; ++h) {
         float dot = 0.f;
         for (int c = 0; c < dI; ++c) dot = fmaf(qs[h * dI + c], __ldg(kr + c), dot);
-        const float sq = q_scale ? qs[HI * dI + h] : 1.f;
-        s = fmaf(sq * sk, dot, s);
+        if (relu) dot = fmaxf(dot, 0.f);
+        s = fmaf(qs[HI * dI + h] * sk, dot, s);
     }
     if (score_bf16) reinterpret_cast<__nv_bfloat16*>(scores)[(long long)r * Nc + j] = __float2bfloat16_rn(s);
     else reinterpret_cast<float*>(scores)[(long long)r * Nc + j] = s;
@@ -358,23 +372,26 @@ cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
-                               void* scores, bool score_bf16, int B, int n_q_total, int i_start, int n_q_rows,
-                               long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s)
+cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* head_w, bool relu,
+                               const float* k, const float* k_scale, void* scores, bool score_bf16, int B,
+                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int HI,
+                               int dI, cudaStream_t s)
 {
     if (B * n_q_rows == 0 || Nc == 0) return cudaSuccess;
     dim3 grid((Nc + 255) / 256, B * n_q_rows);
     size_t smem = (size_t)(HI * dI + HI) * sizeof(float);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(indexer_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    indexer_f32_kernel<<<grid, 256, smem, s>>>(q, q_scale, k, k_scale, scores, score_bf16 ? 1 : 0, n_q_total,
-                                               i_start, n_q_rows, q_pos0, m, Nc, HI, dI);
+    indexer_f32_kernel<<<grid, 256, smem, s>>>(q, q_scale, head_w, relu ? 1 : 0, k, k_scale, scores,
+                                               score_bf16 ? 1 : 0, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, HI,
+                                               dI);
     return cudaGetLastError();
 }
 
 template <bool FP8, int T, bool WMAX>
-static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const float* q_scale,
-                             const float* k_scale, void* scores, bool score_bf16, int B, int n_q_total, int i_start,
+static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const float* q_scale, const float* head_w,
+                             bool relu, const float* k_scale, void* scores, bool score_bf16, int B, int n_q_total,
+                             int i_start,
                              int n_q_rows, long long q_pos0, int m, int Nc, int num_sms, uint32_t* wmax,
                              int wmax_ld, cudaStream_t s)
 {
@@ -393,27 +410,29 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     auto kern = indexer_tc_kernel<FP8, T, WMAX>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     dim3 grid(n_groups * splits, B);
-    kern<<<grid, idx::threads<T>(), C::SMEM, s>>>(tq, tk, q_scale, k_scale, scores, score_bf16 ? 1 : 0, n_q_total,
+    kern<<<grid, idx::threads<T>(), C::SMEM, s>>>(tq, tk, q_scale, head_w, relu ? 1 : 0, k_scale, scores,
+                                             score_bf16 ? 1 : 0, n_q_total,
                                              i_start, n_q_rows, q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
     return cudaGetLastError();
 }
 
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const float* q_scale, const float* k_scale, void* scores, bool score_bf16, int B,
+                              const float* q_scale, const float* head_w, bool relu, const float* k_scale,
+                              void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
                               int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s)
 {
     if (wmax) {   // decode groups (T = 1) only
         if (T != 1) return cudaErrorInvalidValue;
-        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
-        return launch_tc<false, 1, true>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        return launch_tc<false, 1, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
     }
     if (fp8) {
-        if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
-        return launch_tc<true, 1, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+        if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+        return launch_tc<true, 1, false>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
     }
-    if (T == 4) return launch_tc<false, 4, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
-    return launch_tc<false, 1, false>(tq, tk, q_scale, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+    if (T == 4) return launch_tc<false, 4, false>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
+    return launch_tc<false, 1, false>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
 }
 
 int indexer_group_tokens(int n_q) { return n_q >= 4 ? 4 : 1; }

@@ -21,6 +21,10 @@ csa_status_t report(csa_status_t st, const char* msg);
 // out_kind: 0 f32, 1 bf16, 2 e4m3 (+ fp32 row scale), 3 e2m1 (+ e4m3 block scales)
 cudaError_t launch_compress(int B, int n, int m, int d, const float* logits, const void* x, bool x_bf16,
                             void* out, int out_kind, void* out_scale, int num_sms, cudaStream_t s);
+// Per-channel compression weights: logits [B, n, d] (one logit per token and
+// channel); out_kind as above.
+cudaError_t launch_compress_per_channel(int B, int n, int m, int d, const float* logits, const void* x, bool x_bf16,
+                                        void* out, int out_kind, void* out_scale, cudaStream_t s);
 // All streams in one launch, for short blocks (4 <= m <= 32, m and n multiples
 // of 4, one tile entry within the stage budget); out_kind 0 f32, 1 bf16,
 // 2 e4m3, 3 e2m1.
@@ -57,12 +61,16 @@ int indexer_box_rows(int T);
 // (b * n_q_rows + i of the chunk), the largest score key (score_key) of every
 // 32 consecutive visible entries j to wmax[row * wmax_ld + j / 32].
 // scores: fp32, or bf16 (nearest even) when score_bf16.
+// head_w ([B, n_q, H_I] or null) and relu: the weighted / ReLU variant,
+// s = sk * sum_h w_h sq_h max(<q_h, k>, 0).
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const float* q_scale, const float* k_scale, void* scores, bool score_bf16, int B,
+                              const float* q_scale, const float* head_w, bool relu, const float* k_scale,
+                              void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
                               int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s);
-cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* k, const float* k_scale,
-                               void* scores, bool score_bf16, int B, int n_q_total, int i_start, int n_q_rows,
+cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* head_w, bool relu,
+                               const float* k, const float* k_scale, void* scores, bool score_bf16, int B,
+                               int n_q_total, int i_start, int n_q_rows,
                                long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s);
 cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t* x8, float* S,
                                long long rows, int d, cudaStream_t s);
@@ -81,8 +89,12 @@ template <typename TIO> struct AttnArgsT {
     float scale_log2;    // softmax scale * log2(e)
     int mode;            // 0 sparse, 1 closed blocks, 2 window
     int B, n_q, N_kv, k, m, n_splits;
+    // KV heads: K / V are [B, N_kv, H_kv, D]; query head h (of H_tot) reads KV
+    // head h / G, G = H_tot / H_kv.  (1, H_tot, H_tot) is one shared KV head.
+    int H_kv = 1, H_tot = 0, G = 0;
 };
 bool attn_simt_supported(int H, int D);
+// H: query heads per KV head (G); a.H_tot, a.H_kv, a.G describe the layout.
 template <typename TIO>
 cudaError_t launch_attn_simt(const AttnArgsT<TIO>& a, int H, int D, cudaStream_t s);
 // merges split partials (a.part_o, a.part_ml) into a.out / a.lse

@@ -20,7 +20,7 @@ F32, BF16, E4M3, E2M1 = 0, 1, 2, 3
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "WORKSPACE",
           5: "CUDA", 6: "TIMEOUT", 7: "DEVICE"}
 
-EXPORTS = ("csa_compress", "csa_index_scores_workspace_size", "csa_index_scores",
+EXPORTS = ("csa_compress", "csa_compress_per_channel", "csa_index_scores_workspace_size", "csa_index_scores",
            "csa_topk_select_workspace_size", "csa_topk_select", "csa_topk_select_noalloc",
            "csa_index_topk_workspace_size",
            "csa_index_topk", "csa_sparse_attn_workspace_size", "csa_sparse_attn", "hca_attn",
@@ -47,17 +47,18 @@ def load():
     lib = C.CDLL(LIB_PATH)
     sig = {
         "csa_compress": ([_I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P], _I),
+        "csa_compress_per_channel": ([_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
         "csa_index_scores_workspace_size": ([_I, _I, _I, _I], _S),
-        "csa_index_scores": ([_I, _I, _L, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _I, _P, _S, _P], _I),
+        "csa_index_scores": ([_I, _I, _L, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _I, _P, _I, _P, _S, _P], _I),
         "csa_topk_select_workspace_size": ([_I, _I, _I, _I], _S),
         "csa_topk_select": ([_I, _I, _L, _I, _I, _I, _P, _I, _P, _P, _S, _P], _I),
         "csa_topk_select_noalloc": ([_I, _I, _L, _I, _I, _I, _P, _P, _P], _I),
         "csa_index_topk_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _S),
-        "csa_index_topk": ([_I, _I, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _I, _P, _P, _S, _P], _I),
+        "csa_index_topk": ([_I, _I, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _S, _P], _I),
         "csa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I], _S),
-        "csa_sparse_attn": ([_I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P], _I),
-        "hca_attn": ([_I, _I, _L, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
-        "swa_attn": ([_I, _I, _L, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
+        "csa_sparse_attn": ([_I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P], _I),
+        "hca_attn": ([_I, _I, _L, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
+        "swa_attn": ([_I, _I, _L, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
         "csa_device_status": ([_P], _I),
         "csa_last_error": ([], C.c_char_p),
         "csa_wait_selftest": ([C.c_uint32, _P, _P], _I),
@@ -104,16 +105,29 @@ def csa_compress(B, n, m, logits, xs, x_dtypes, dims, outs, out_dtypes, out_scal
                                op, _arr(C.c_int, out_dtypes), sp, _stream(stream)))
 
 
+def csa_compress_per_channel(B, n, m, logits, xs, x_dtypes, dims, outs, out_dtypes, out_scales=None, stream=None):
+    """logits: one [B, n, dim] fp32 tensor per stream."""
+    ns = len(xs)
+    lp = _arr(C.c_void_p, [_ptr(lg) for lg in logits])
+    xp = _arr(C.c_void_p, [_ptr(x) for x in xs])
+    op = _arr(C.c_void_p, [_ptr(o) for o in outs])
+    sp = None if out_scales is None else _arr(C.c_void_p, [_ptr(s) for s in out_scales])
+    _check(load().csa_compress_per_channel(B, n, m, ns, lp, xp, _arr(C.c_int, x_dtypes), _arr(C.c_int, dims), op,
+                                           _arr(C.c_int, out_dtypes), sp, _stream(stream)))
+
+
 def csa_index_scores_workspace_size(B, N_c, d_I, k_dtype):
     return load().csa_index_scores_workspace_size(B, N_c, d_I, k_dtype)
 
 
 def csa_index_scores(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                     scores, workspace=None, workspace_bytes=0, stream=None):
-    """scores: an fp32 or bf16 tensor; its dtype is the score_dtype passed on."""
+                     scores, workspace=None, workspace_bytes=0, stream=None, head_weight=None, relu=False):
+    """scores: an fp32 or bf16 tensor; its dtype is the score_dtype passed on.
+    head_weight / relu (keywords) are the C arguments that follow k_scale."""
     _check(load().csa_index_scores(B, n_q, q_pos0, m, N_c, H_I, d_I, _ptr(q_idx), q_dtype, _ptr(q_scale),
-                                   _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(scores), dtype_code(scores.dtype),
-                                   _ptr(workspace), workspace_bytes, _stream(stream)))
+                                   _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(head_weight), 1 if relu else 0,
+                                   _ptr(scores), dtype_code(scores.dtype), _ptr(workspace), workspace_bytes,
+                                   _stream(stream)))
 
 
 def csa_topk_select_workspace_size(B, n_q, N_c, k):
@@ -140,11 +154,12 @@ def csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype, score_dtype
 
 
 def csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                   topk, workspace, workspace_bytes, stream=None, score_dtype=F32):
-    """score_dtype (keyword; F32 or BF16) is the C argument that precedes topk."""
+                   topk, workspace, workspace_bytes, stream=None, score_dtype=F32, head_weight=None, relu=False):
+    """head_weight, relu and score_dtype (keywords) are the C arguments
+    between k_scale and topk."""
     _check(load().csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, _ptr(q_idx), q_dtype, _ptr(q_scale),
-                                 _ptr(k_idx), k_dtype, _ptr(k_scale), score_dtype, _ptr(topk), _ptr(workspace),
-                                 workspace_bytes, _stream(stream)))
+                                 _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(head_weight), 1 if relu else 0,
+                                 score_dtype, _ptr(topk), _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def csa_sparse_attn_workspace_size(B, n_q, H, d, k):
@@ -152,19 +167,23 @@ def csa_sparse_attn_workspace_size(B, n_q, H, d, k):
 
 
 def csa_sparse_attn(B, n_q, H, d, N_c, k, scale, q, k_c, v_c, dtype, topk, out, lse=None, workspace=None,
-                    workspace_bytes=0, stream=None):
-    _check(load().csa_sparse_attn(B, n_q, H, d, N_c, k, scale, _ptr(q), _ptr(k_c), _ptr(v_c), dtype, _ptr(topk),
-                                  _ptr(out), _ptr(lse), _ptr(workspace), workspace_bytes, _stream(stream)))
+                    workspace_bytes=0, stream=None, H_kv=1):
+    """H_kv (keyword) is the C argument after H."""
+    _check(load().csa_sparse_attn(B, n_q, H, H_kv, d, N_c, k, scale, _ptr(q), _ptr(k_c), _ptr(v_c), dtype,
+                                  _ptr(topk), _ptr(out), _ptr(lse), _ptr(workspace), workspace_bytes,
+                                  _stream(stream)))
 
 
-def hca_attn(B, n_q, q_pos0, m, N_c, H, d, scale, q, k_c, v_c, dtype, out, lse=None, stream=None):
-    _check(load().hca_attn(B, n_q, q_pos0, m, N_c, H, d, scale, _ptr(q), _ptr(k_c), _ptr(v_c), dtype, _ptr(out),
-                           _ptr(lse), _stream(stream)))
+def hca_attn(B, n_q, q_pos0, m, N_c, H, d, scale, q, k_c, v_c, dtype, out, lse=None, stream=None, H_kv=1):
+    """H_kv (keyword) is the C argument after H."""
+    _check(load().hca_attn(B, n_q, q_pos0, m, N_c, H, H_kv, d, scale, _ptr(q), _ptr(k_c), _ptr(v_c), dtype,
+                           _ptr(out), _ptr(lse), _stream(stream)))
 
 
-def swa_attn(B, n_q, q_pos0, n_kv, window, H, d, scale, q, k, v, dtype, out, lse=None, stream=None):
-    _check(load().swa_attn(B, n_q, q_pos0, n_kv, window, H, d, scale, _ptr(q), _ptr(k), _ptr(v), dtype, _ptr(out),
-                           _ptr(lse), _stream(stream)))
+def swa_attn(B, n_q, q_pos0, n_kv, window, H, d, scale, q, k, v, dtype, out, lse=None, stream=None, H_kv=1):
+    """H_kv (keyword) is the C argument after H."""
+    _check(load().swa_attn(B, n_q, q_pos0, n_kv, window, H, H_kv, d, scale, _ptr(q), _ptr(k), _ptr(v), dtype,
+                           _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def csa_device_status(stream=None):

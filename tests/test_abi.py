@@ -42,21 +42,21 @@ def test_host_side_validation_without_gpu():
     st = L.csa_compress(1, 16, 0, None, 1, None, None, None, None, None, None, None)
     assert st == 1 and "m=0" in L.csa_last_error().decode()
     st = L.csa_index_scores(1, 4, 0, 4, 8, 64, 128, None, lib.BF16, None, None, lib.E4M3, None,
-                            None, lib.F32, None, 0, None)
+                            None, 0, None, lib.F32, None, 0, None)
     assert st == 2
     st = L.csa_index_scores(1, 4, 0, 4, 8, 32, 128, None, lib.BF16, None, None, lib.BF16, None,
-                            None, lib.F32, None, 0, None)
+                            None, 0, None, lib.F32, None, 0, None)
     assert st == 2 and "H_I=64" in L.csa_last_error().decode()
     st = L.csa_topk_select(1, 1, 0, 1, 10, 0, None, lib.F32, None, None, 0, None)
     assert st == 2
-    st = L.hca_attn(1, 1, 0, 4, 8, 12, 128, 0.1, None, None, None, lib.BF16, None, None, None)
+    st = L.hca_attn(1, 1, 0, 4, 8, 12, 1, 128, 0.1, None, None, None, lib.BF16, None, None, None)
     assert st == 2
     # the softmax scale must be positive and finite
     for bad in (0.0, -0.5, float("inf"), float("nan")):
-        st = L.hca_attn(1, 1, 0, 4, 8, 64, 128, bad, None, None, None, lib.BF16, None, None, None)
+        st = L.hca_attn(1, 1, 0, 4, 8, 64, 1, 128, bad, None, None, None, lib.BF16, None, None, None)
         assert st == 1 and "scale" in L.csa_last_error().decode()
     # misaligned pointer
-    st = L.swa_attn(1, 1, 0, 8, 4, 8, 64, 0.1, 8, 16, 16, lib.F32, 16, None, None)
+    st = L.swa_attn(1, 1, 0, 8, 4, 8, 1, 64, 0.1, 8, 16, 16, lib.F32, 16, None, None)
     assert st == 3
 
 
