@@ -202,6 +202,54 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
                             size_t workspace_bytes, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * csa_index_topk_varlen -- csa_index_topk for sequences of different lengths
+ * held on the device: query i of sequence b sits at position
+ * lens[b] - n_q + i (lens: device int64 [B], the tokens of each sequence
+ * including its n_q queries -- the counts csa_decode_append keeps).  N_c is
+ * the caches' capacity (entries per sequence); sequence b sees its first
+ * min(floor((lens[b] - n_q + i + 1) / m), N_c) entries (none where that
+ * position is negative: lens[b] < n_q).  Other arguments,
+ * outputs and the workspace as in csa_index_topk.
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_index_topk_varlen(int B, int n_q, const int64_t* lens, int m, int N_c, int H_I, int d_I,
+                                   int k, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale,
+                                   const void* k_idx, csa_dtype_t k_dtype, const void* k_scale,
+                                   const float* head_weight, int relu,
+                                   csa_dtype_t score_dtype, int32_t* topk, void* workspace,
+                                   size_t workspace_bytes, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * csa_decode_append -- streaming decode state: the KV-cache compression of
+ * "DeepSeek V4 技术解读" §2.1 (every m tokens merged into one entry) applied
+ * one generated token at a time.  For every sequence b (t = lens[b] tokens
+ * so far): the new token (its logit, K, V and indexer-K rows) is written to
+ * slot t % m of the sequence's open block (the stage buffers), lens[b]
+ * becomes t + 1, and when t + 1 is a multiple of m the block is compressed
+ * -- softmax of its m logits, fp32 sums in token order, the quantising
+ * epilogue of csa_compress -- into entry (t + 1) / m - 1 of the caches.
+ *   logit_new fp32 [B]; k_new, v_new [B, d]; ik_new [B, d_I]  (x_dtype:
+ *             CSA_F32 or CSA_BF16), device;
+ *   stage_logits fp32 [B, m]; stage_k, stage_v [B, m, d]; stage_ik
+ *             [B, m, d_I] (x_dtype): the open blocks, caller-owned, device;
+ *   lens      device int64 [B], advanced by one;
+ *   k_c, v_c  device [B, N_cap, d] in kv_dtype (CSA_F32 or CSA_BF16);
+ *   ik_c, ik_scale  indexer-key cache [B, N_cap, d_I] in ik_dtype: CSA_F32 /
+ *             CSA_BF16 (ik_scale unused), CSA_E4M3 (ik_scale fp32 [B, N_cap]),
+ *             or CSA_E2M1 (packed [B, N_cap, d_I / 2], ik_scale E4M3
+ *             [B, N_cap, d_I / 32]).
+ * Requirements: 1 <= m <= 128, d and d_I <= 256, d_I even (a multiple of 32
+ * for E2M1).  A block closing past N_cap entries is not written, and a
+ * negative lens[b] leaves sequence b untouched; both flag CSA_ERR_DEVICE in
+ * the status word.  Deterministic; sequences are
+ * independent (one CTA each).
+ * ------------------------------------------------------------------------- */
+csa_status_t csa_decode_append(int B, int m, int d, int d_I, int64_t N_cap, const float* logit_new,
+                               const void* k_new, const void* v_new, const void* ik_new, csa_dtype_t x_dtype,
+                               float* stage_logits, void* stage_k, void* stage_v, void* stage_ik,
+                               int64_t* lens, void* k_c, void* v_c, csa_dtype_t kv_dtype, void* ik_c,
+                               csa_dtype_t ik_dtype, void* ik_scale, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * csa_sparse_attn -- CSA core attention ("DeepSeek V4 技术解读" §2.1 Core
  * Attention: full attention over only the k selected entries):
  *     o[b,i,h,:] = sum_{j in topk[b,i,:], j >= 0} softmax_j(scale * <q, k_c[b,j]>) v_c[b,j,:]

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsa_b300.so")
-SOURCES = ["api.cu", "compress.cu", "indexer.cu", "topk.cu", "topk_noalloc.cu", "attn.cu", "attn_tc.cu"]
+SOURCES = ["api.cu", "compress.cu", "indexer.cu", "topk.cu", "topk_noalloc.cu", "attn.cu", "attn_tc.cu", "decode.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

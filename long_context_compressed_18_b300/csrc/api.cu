@@ -133,7 +133,7 @@ SplitPlan attn_split_plan(int n_q, long long set_len)
 
 // wmax non-null: the tensor-core decode kernel also writes each row's warp
 // maxima there (the top-k's collection threshold).
-csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, int64_t q_pos0, int m, int N_c, int H_I,
+csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, QPos q_pos0, int m, int N_c, int H_I,
                         int d_I, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
                         csa_dtype_t k_dtype, const void* k_scale, const float* head_w, bool relu, void* scores,
                         bool sbf16, void* ws, cudaStream_t s, uint32_t* wmax = nullptr, int wmax_ld = 0)
@@ -480,6 +480,37 @@ csa_status_t csa_compress_per_channel(int B, int n, int m, int n_streams, const 
     return CSA_OK;
 }
 
+csa_status_t csa_decode_append(int B, int m, int d, int d_I, int64_t N_cap, const float* logit_new,
+                               const void* k_new, const void* v_new, const void* ik_new, csa_dtype_t x_dtype,
+                               float* stage_logits, void* stage_k, void* stage_v, void* stage_ik, int64_t* lens,
+                               void* k_c, void* v_c, csa_dtype_t kv_dtype, void* ik_c, csa_dtype_t ik_dtype,
+                               void* ik_scale, csa_stream_t stream)
+{
+    if (B < 0 || m < 1 || N_cap < 0) return fail(CSA_ERR_INVALID_ARG, "bad sizes B=%d m=%d", B, m);
+    if (m > DECODE_MAX_M) return fail(CSA_ERR_UNSUPPORTED, "decode append needs m <= %d", DECODE_MAX_M);
+    if (d < 1 || d > DECODE_MAX_DIM || d_I < 2 || d_I > DECODE_MAX_DIM || (d_I & 1))
+        return fail(CSA_ERR_UNSUPPORTED, "decode append needs d, d_I <= %d (d_I even)", DECODE_MAX_DIM);
+    if (x_dtype != CSA_F32 && x_dtype != CSA_BF16) return fail(CSA_ERR_INVALID_ARG, "new tokens must be F32 or BF16");
+    if (kv_dtype != CSA_F32 && kv_dtype != CSA_BF16) return fail(CSA_ERR_INVALID_ARG, "K/V caches must be F32 or BF16");
+    if (ik_dtype == CSA_E2M1 && d_I % 32) return fail(CSA_ERR_UNSUPPORTED, "E2M1 indexer keys need d_I % 32 == 0");
+    if (B == 0) return CSA_OK;
+    const void* ptrs[] = {logit_new, k_new, v_new, ik_new, stage_logits, stage_k, stage_v, stage_ik, lens, k_c, v_c, ik_c};
+    for (const void* p : ptrs)
+        if (!p || !aligned16(p)) return fail(CSA_ERR_ALIGNMENT, "decode append: pointer NULL or not 16-byte aligned");
+    if ((ik_dtype == CSA_E4M3 || ik_dtype == CSA_E2M1) && (!ik_scale || !aligned16(ik_scale)))
+        return fail(CSA_ERR_INVALID_ARG, "quantised indexer keys need an aligned ik_scale");
+    DecodeAppendArgs a{};
+    a.B = B; a.m = m; a.d = d; a.d_I = d_I; a.N_cap = N_cap;
+    a.logit_new = logit_new; a.k_new = k_new; a.v_new = v_new; a.ik_new = ik_new;
+    a.st_logit = stage_logits; a.st_k = stage_k; a.st_v = stage_v; a.st_ik = stage_ik;
+    a.lens = reinterpret_cast<long long*>(lens);
+    a.k_c = k_c; a.v_c = v_c; a.kv_kind = kv_dtype == CSA_BF16 ? 1 : 0;
+    a.ik_c = ik_c; a.ik_scale = ik_scale;
+    a.ik_kind = ik_dtype == CSA_F32 ? 0 : ik_dtype == CSA_BF16 ? 1 : ik_dtype == CSA_E4M3 ? 2 : 3;
+    return cuda_status(launch_decode_append(a, x_dtype == CSA_BF16, reinterpret_cast<cudaStream_t>(stream)),
+                       "decode append launch");
+}
+
 size_t csa_index_scores_workspace_size(int B, int N_c, int d_I, csa_dtype_t k_dtype)
 {
     if (B < 0 || N_c < 0 || d_I < 0) return 0;
@@ -547,11 +578,13 @@ size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, 
            (topk_long_rows(N_c, k) ? topk_wmax_bytes((long long)B * rows, N_c) : 0);
 }
 
-csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
-                            const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
-                            csa_dtype_t k_dtype, const void* k_scale, const float* head_weight, int relu,
-                            csa_dtype_t score_dtype, int32_t* topk, void* workspace, size_t workspace_bytes,
-                            csa_stream_t stream)
+// csa_index_topk and csa_index_topk_varlen: positions are q_pos0 for every
+// sequence, or (lens non-null) lens[b] - n_q for sequence b.
+static csa_status_t index_topk_impl(int B, int n_q, int64_t q_pos0, const int64_t* lens, int m, int N_c, int H_I,
+                                    int d_I, int k, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale,
+                                    const void* k_idx, csa_dtype_t k_dtype, const void* k_scale,
+                                    const float* head_weight, int relu, csa_dtype_t score_dtype, int32_t* topk,
+                                    void* workspace, size_t workspace_bytes, csa_stream_t stream)
 {
     csa_status_t st = check_index_args(B, n_q, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
                                        head_weight);
@@ -569,7 +602,10 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
     const size_t need = csa_index_topk_workspace_size(B, n_q, N_c, H_I, d_I, k, k_dtype, score_dtype);
     if (!workspace || workspace_bytes < need || !aligned16(workspace))
         return fail(CSA_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+    if (lens && !aligned16(lens)) return fail(CSA_ERR_ALIGNMENT, "lens not 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the scores' positions (the indexer adds the chunk's first row itself)
+    const QPos qp = lens ? QPos(reinterpret_cast<const long long*>(lens), -(long long)n_q) : QPos(q_pos0);
     const int rows = index_chunk_rows(B, n_q, N_c, esz);
     uint8_t* w = reinterpret_cast<uint8_t*>(workspace);
     void* scores = w;
@@ -582,25 +618,46 @@ csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int 
             // scores plus the rows' warp maxima in one kernel, then the top-k
             // with its collection threshold taken from them
             const int ld = topk_wmax_ld(N_c);
-            st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+            st = run_scores(B, n_q, i0, nr, qp, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
                             head_weight, relu != 0, scores, sbf16, w_scores_ws, s, w_wmax, ld);
             if (st != CSA_OK) return st;
-            st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q,
+            st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, qp.shifted(i0), m, N_c, k, topk + (size_t)i0 * k, n_q,
                                          w_topk, s, w_wmax, ld),
                              "topk launch");
             if (st != CSA_OK) return st;
             continue;
         }
         if (N_c > 0) {
-            st = run_scores(B, n_q, i0, nr, q_pos0, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+            st = run_scores(B, n_q, i0, nr, qp, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
                             head_weight, relu != 0, scores, sbf16, w_scores_ws, s);
             if (st != CSA_OK) return st;
         }
-        st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, q_pos0 + i0, m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk, s),
+        st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, qp.shifted(i0), m, N_c, k, topk + (size_t)i0 * k, n_q, w_topk, s),
                          "topk launch");
         if (st != CSA_OK) return st;
     }
     return CSA_OK;
+}
+
+csa_status_t csa_index_topk(int B, int n_q, int64_t q_pos0, int m, int N_c, int H_I, int d_I, int k,
+                            const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
+                            csa_dtype_t k_dtype, const void* k_scale, const float* head_weight, int relu,
+                            csa_dtype_t score_dtype, int32_t* topk, void* workspace, size_t workspace_bytes,
+                            csa_stream_t stream)
+{
+    return index_topk_impl(B, n_q, q_pos0, nullptr, m, N_c, H_I, d_I, k, q_idx, q_dtype, q_scale, k_idx, k_dtype,
+                           k_scale, head_weight, relu, score_dtype, topk, workspace, workspace_bytes, stream);
+}
+
+csa_status_t csa_index_topk_varlen(int B, int n_q, const int64_t* lens, int m, int N_c, int H_I, int d_I, int k,
+                                   const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
+                                   csa_dtype_t k_dtype, const void* k_scale, const float* head_weight, int relu,
+                                   csa_dtype_t score_dtype, int32_t* topk, void* workspace, size_t workspace_bytes,
+                                   csa_stream_t stream)
+{
+    if (!lens && (long long)B * n_q > 0) return fail(CSA_ERR_INVALID_ARG, "lens is NULL");
+    return index_topk_impl(B, n_q, 0, lens, m, N_c, H_I, d_I, k, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+                           head_weight, relu, score_dtype, topk, workspace, workspace_bytes, stream);
 }
 
 size_t csa_sparse_attn_workspace_size(int B, int n_q, int H, int d, int k)

@@ -110,7 +110,7 @@ template <bool FP8, int T, bool WMAX>
 __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const float* __restrict__ q_scale, const float* __restrict__ head_w, int relu, const float* __restrict__ k_scale,
-    void* __restrict__ scores, int score_bf16, int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m,
+    void* __restrict__ scores, int score_bf16, int n_q_total, int i_start, int n_q_rows, QPos qp, int m,
     int Nc, int n_splits, int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
 {
     using C = idx::Cfg<FP8, T>;
@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
     const int g = blockIdx.x / n_splits, split = blockIdx.x % n_splits;
     const int i0 = g * T;                                   // first token of the group (chunk-local)
     const int i_last = min(i0 + T - 1, n_q_rows - 1);
+    const long long q_pos0 = qp.at(blockIdx.y);   // this sequence's first query position
     long long nvl = (q_pos0 + i_start + i_last + 1) / m;
     const int nv_last = (int)(nvl < Nc ? nvl : Nc);
     const int total_tiles = (nv_last + idx::BLOCK_KEYS - 1) / idx::BLOCK_KEYS;
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(idx::threads<T>(), 1) indexer_tc_kernel(
 __global__ void __launch_bounds__(256) indexer_f32_kernel(
     const float* __restrict__ q, const float* __restrict__ q_scale, const float* __restrict__ head_w, int relu,
     const float* __restrict__ k, const float* __restrict__ k_scale, void* __restrict__ scores, int score_bf16,
-    int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int HI, int dI)
+    int n_q_total, int i_start, int n_q_rows, QPos qp, int m, int Nc, int HI, int dI)
 {
     extern __shared__ float qs[];
     const int r = blockIdx.y;          // chunk-local row = b * n_q_rows + i
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(256) indexer_f32_kernel(
     for (int x = threadIdx.x; x < HI; x += blockDim.x)
         qs[HI * dI + x] = (q_scale ? q_scale[qrow * HI + x] : 1.f) * (head_w ? head_w[qrow * HI + x] : 1.f);
     __syncthreads();
-    long long nvl = (q_pos0 + i_start + i + 1) / m;
+    long long nvl = (qp.at(b) + i_start + i + 1) / m;
     const int nv = (int)(nvl < Nc ? nvl : Nc);
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= nv) return;
@@ -374,7 +375,7 @@ cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t
 
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* head_w, bool relu,
                                const float* k, const float* k_scale, void* scores, bool score_bf16, int B,
-                               int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc, int HI,
+                               int n_q_total, int i_start, int n_q_rows, QPos q_pos0, int m, int Nc, int HI,
                                int dI, cudaStream_t s)
 {
     if (B * n_q_rows == 0 || Nc == 0) return cudaSuccess;
@@ -392,12 +393,13 @@ template <bool FP8, int T, bool WMAX>
 static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const float* q_scale, const float* head_w,
                              bool relu, const float* k_scale, void* scores, bool score_bf16, int B, int n_q_total,
                              int i_start,
-                             int n_q_rows, long long q_pos0, int m, int Nc, int num_sms, uint32_t* wmax,
+                             int n_q_rows, QPos q_pos0, int m, int Nc, int num_sms, uint32_t* wmax,
                              int wmax_ld, cudaStream_t s)
 {
     using C = idx::Cfg<FP8, T>;
     const int n_groups = (n_q_rows + T - 1) / T;
-    long long nv_max = (q_pos0 + i_start + n_q_rows) / m;
+    // per-sequence positions live on the device: cover every entry
+    long long nv_max = q_pos0.lens ? (long long)Nc : (q_pos0.q_pos0 + i_start + n_q_rows) / m;
     if (nv_max > Nc) nv_max = Nc;
     const int tiles = (int)((nv_max + idx::BLOCK_KEYS - 1) / idx::BLOCK_KEYS);
     if (tiles == 0 || n_groups == 0) return cudaSuccess;
@@ -419,7 +421,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
                               const float* q_scale, const float* head_w, bool relu, const float* k_scale,
                               void* scores, bool score_bf16, int B,
-                              int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
+                              int n_q_total, int i_start, int n_q_rows, QPos q_pos0, int m, int Nc,
                               int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s)
 {
     if (wmax) {   // decode groups (T = 1) only

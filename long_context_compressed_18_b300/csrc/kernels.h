@@ -33,6 +33,45 @@ cudaError_t launch_compress_tiles(int B, int n, int m, int n_streams, const floa
                                   const bool* x_bf16, const int* dim, void* const* out, const int* out_kind,
                                   void* const* out_scale, int num_sms, cudaStream_t s);
 
+// Query positions: query i of sequence b sits at at(b) + i, where at(b) is
+// q_pos0, or lens[b] + off when per-sequence token counts (a device array)
+// are given.  at() with lens reads device memory: device code only.
+struct QPos {
+    long long q_pos0 = 0;
+    const long long* lens = nullptr;
+    long long off = 0;
+    QPos() = default;
+    QPos(long long p) : q_pos0(p) {}   // NOLINT: a single start for every sequence
+    QPos(const long long* l, long long o) : lens(l), off(o) {}
+    __device__ __forceinline__ long long at(long long b) const { return lens ? lens[b] + off : q_pos0; }
+    // the same positions shifted by i0 queries (a chunk of rows)
+    QPos shifted(long long i0) const { QPos q = *this; q.q_pos0 += i0; q.off += i0; return q; }
+};
+
+// ---- streaming decode state ----
+constexpr int DECODE_MAX_M = 128;     // longest block (HCA's m' = 128)
+constexpr int DECODE_MAX_DIM = 256;
+struct DecodeAppendArgs {
+    int B, m, d, d_I;
+    long long N_cap;                  // entries each sequence's caches hold
+    const float* logit_new;           // [B]
+    const void* k_new;                // [B, d]   (input dtype)
+    const void* v_new;                // [B, d]
+    const void* ik_new;               // [B, d_I]
+    float* st_logit;                  // [B, m]   the open block, raw tokens
+    void* st_k;                       // [B, m, d]
+    void* st_v;                       // [B, m, d]
+    void* st_ik;                      // [B, m, d_I]
+    long long* lens;                  // [B] tokens appended so far (advanced)
+    void* k_c;                        // [B, N_cap, d]
+    void* v_c;                        // [B, N_cap, d]
+    int kv_kind;                      // 0 fp32, 1 bf16
+    void* ik_c;                       // [B, N_cap, d_I] (E2M1: d_I / 2 bytes a row)
+    void* ik_scale;                   // E4M3: fp32 [B, N_cap]; E2M1: E4M3 [B, N_cap, d_I / 32]
+    int ik_kind;                      // 0 fp32, 1 bf16, 2 e4m3, 3 e2m1
+};
+cudaError_t launch_decode_append(const DecodeAppendArgs& a, bool x_bf16, cudaStream_t s);
+
 // ---- top-k ----
 constexpr int TOPK_MAX_SINGLE = 32768;   // entries one CTA selects from (keys in smem)
 constexpr int TOPK_MAX_ROW = 524288;     // longest row (the select kernel's bitmaps)
@@ -47,7 +86,7 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k);
 // row), written by the decode indexer; the collection then takes its
 // threshold from them instead of from a sample of the row.
 // scores: fp32, or bf16 when scores_bf16 (selection on the stored values).
-cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, long long q_pos0,
+cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, QPos q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
                         cudaStream_t s, const uint32_t* wmax = nullptr, int wmax_ld = 0);
 bool topk_long_rows(int N_c, int k);
@@ -66,12 +105,12 @@ int indexer_box_rows(int T);
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
                               const float* q_scale, const float* head_w, bool relu, const float* k_scale,
                               void* scores, bool score_bf16, int B,
-                              int n_q_total, int i_start, int n_q_rows, long long q_pos0, int m, int Nc,
+                              int n_q_total, int i_start, int n_q_rows, QPos q_pos0, int m, int Nc,
                               int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s);
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* head_w, bool relu,
                                const float* k, const float* k_scale, void* scores, bool score_bf16, int B,
                                int n_q_total, int i_start, int n_q_rows,
-                               long long q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s);
+                               QPos q_pos0, int m, int Nc, int HI, int dI, cudaStream_t s);
 cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t* x8, float* S,
                                long long rows, int d, cudaStream_t s);
 

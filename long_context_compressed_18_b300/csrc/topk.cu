@@ -268,7 +268,7 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
 // writes the final indices, -1 padded.
 template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
-    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc,
     int k, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
     const int r = (int)blockIdx.x;
     const int i = r % n_q_rows;   // query index within the chunk of rows
     const long long out_row = (long long)(r / n_q_rows) * out_b_stride + i;
-    long long nvl = (q_pos0 + i + 1) / m;
+    long long nvl = (qp.at(r / n_q_rows) + i + 1) / m;
     const int len = (int)(nvl < Nc ? nvl : Nc);
     const int tid = threadIdx.x;
     const int kk = min(k, len);
@@ -349,7 +349,8 @@ static LongRowWs lr_ws(void* ws, long long rows, int k)
 
 __device__ __forceinline__ int visible_len(long long q_pos0, int i, int m, int Nc)
 {
-    const long long nvl = (q_pos0 + i + 1) / m;
+    const long long t1 = q_pos0 + i + 1;             // negative positions (a short sequence) see nothing
+    const long long nvl = t1 > 0 ? t1 / m : 0;
     return (int)(nvl < Nc ? nvl : Nc);
 }
 
@@ -600,7 +601,7 @@ __device__ uint32_t wmax_threshold(const uint32_t* __restrict__ wrow, int nw, in
 
 template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
-    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k,
     int n_chunks, LongRowWs w, const uint32_t* __restrict__ wmax, int wmax_ld)
 {
     // the chunk's entries go to a shared-memory list, then one global atomic
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
     uint32_t* lkey = reinterpret_cast<uint32_t*>(smem_raw);   // [LR_LOCAL_CAP]
     int32_t* lidx = reinterpret_cast<int32_t*>(lkey + LR_LOCAL_CAP);
     const int r = blockIdx.x / n_chunks, c = blockIdx.x % n_chunks;
-    const int L = visible_len(q_pos0, r % n_q_rows, m, Nc);
+    const int L = visible_len(qp.at(r / n_q_rows), r % n_q_rows, m, Nc);
     if (L <= k) return;
     const int c0 = c * LR_CHUNK, len = max(0, min(LR_CHUNK, L - c0));
     if (len == 0) return;
@@ -843,7 +844,7 @@ __device__ void select_streaming(const ST* __restrict__ row, int L, int kk, Topk
 
 template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
-    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k,
     LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -851,7 +852,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const int r = blockIdx.x;
     const int i = r % n_q_rows;
     int32_t* o = out + ((long long)(r / n_q_rows) * out_b_stride + i) * k;
-    const int L = visible_len(q_pos0, i, m, Nc);
+    const int L = visible_len(qp.at(r / n_q_rows), i, m, Nc);
     const int kk = min(k, L);
     const int tid = threadIdx.x;
     for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
@@ -914,7 +915,7 @@ static size_t row_smem_bytes(int N_c, int k) { return (size_t)row_cap(N_c, k) * 
 
 template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
-    const ST* __restrict__ scores, long long ld, int n_q_rows, long long q_pos0, int m, int Nc, int k, int cap,
+    const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k, int cap,
     int32_t* __restrict__ out, long long out_b_stride)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -926,7 +927,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
     const int r = (int)blockIdx.x;
     const int i = r % n_q_rows;   // query index within the chunk of rows
     int32_t* o = out + ((long long)(r / n_q_rows) * out_b_stride + i) * k;
-    const int L = visible_len(q_pos0, i, m, Nc);
+    const int L = visible_len(qp.at(r / n_q_rows), i, m, Nc);
     const int kk = min(k, L);
     const int tid = threadIdx.x;
     for (int p = kk + tid; p < k; p += TOPK_THREADS) o[p] = -1;
@@ -984,7 +985,7 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k)
 // bitmaps of the row and the entry list in shared memory; shapes beyond that
 // stream every row instead.
 template <typename ST>
-static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, long long q_pos0, int m, int N_c,
+static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, QPos q_pos0, int m, int N_c,
                                  int k, const LongRowWs& w, int rows, int32_t* out, long long out_b_stride,
                                  cudaStream_t s)
 {
@@ -998,7 +999,7 @@ static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, l
 }
 
 template <typename ST>
-static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_rows, long long q_pos0, int m,
+static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_rows, QPos q_pos0, int m,
                                  int N_c, int k, int32_t* out, long long out_b_stride, void* ws, cudaStream_t s,
                                  const uint32_t* wmax, int wmax_ld)
 {
@@ -1033,7 +1034,7 @@ static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_
     return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, rows, out, out_b_stride, s);
 }
 
-cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, long long q_pos0,
+cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, QPos q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
                         cudaStream_t s, const uint32_t* wmax, int wmax_ld)
 {

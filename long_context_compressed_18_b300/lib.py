@@ -23,7 +23,7 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "WORKS
 EXPORTS = ("csa_compress", "csa_compress_per_channel", "csa_index_scores_workspace_size", "csa_index_scores",
            "csa_topk_select_workspace_size", "csa_topk_select", "csa_topk_select_noalloc",
            "csa_index_topk_workspace_size",
-           "csa_index_topk", "csa_sparse_attn_workspace_size", "csa_sparse_attn", "hca_attn",
+           "csa_index_topk", "csa_index_topk_varlen", "csa_decode_append", "csa_sparse_attn_workspace_size", "csa_sparse_attn", "hca_attn",
            "swa_attn", "csa_device_status", "csa_last_error", "csa_wait_selftest")
 
 
@@ -55,6 +55,10 @@ def load():
         "csa_topk_select_noalloc": ([_I, _I, _L, _I, _I, _I, _P, _P, _P], _I),
         "csa_index_topk_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _S),
         "csa_index_topk": ([_I, _I, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _S, _P], _I),
+        "csa_index_topk_varlen": ([_I, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _P, _P, _S,
+                                   _P], _I),
+        "csa_decode_append": ([_I, _I, _I, _I, _L, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _P,
+                               _P], _I),
         "csa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I], _S),
         "csa_sparse_attn": ([_I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P], _I),
         "hca_attn": ([_I, _I, _L, _I, _I, _I, _I, _I, _F, _P, _P, _P, _I, _P, _P, _P], _I),
@@ -160,6 +164,24 @@ def csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, q_idx, q_dtype, q_scale,
     _check(load().csa_index_topk(B, n_q, q_pos0, m, N_c, H_I, d_I, k, _ptr(q_idx), q_dtype, _ptr(q_scale),
                                  _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(head_weight), 1 if relu else 0,
                                  score_dtype, _ptr(topk), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def csa_index_topk_varlen(B, n_q, lens, m, N_c, H_I, d_I, k, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
+                          topk, workspace, workspace_bytes, stream=None, score_dtype=F32, head_weight=None,
+                          relu=False):
+    """lens: device int64 [B]; keywords as in csa_index_topk."""
+    _check(load().csa_index_topk_varlen(B, n_q, _ptr(lens), m, N_c, H_I, d_I, k, _ptr(q_idx), q_dtype,
+                                        _ptr(q_scale), _ptr(k_idx), k_dtype, _ptr(k_scale), _ptr(head_weight),
+                                        1 if relu else 0, score_dtype, _ptr(topk), _ptr(workspace),
+                                        workspace_bytes, _stream(stream)))
+
+
+def csa_decode_append(B, m, d, d_I, N_cap, logit_new, k_new, v_new, ik_new, x_dtype, stage_logits, stage_k,
+                      stage_v, stage_ik, lens, k_c, v_c, kv_dtype, ik_c, ik_dtype, ik_scale=None, stream=None):
+    _check(load().csa_decode_append(B, m, d, d_I, N_cap, _ptr(logit_new), _ptr(k_new), _ptr(v_new), _ptr(ik_new),
+                                    x_dtype, _ptr(stage_logits), _ptr(stage_k), _ptr(stage_v), _ptr(stage_ik),
+                                    _ptr(lens), _ptr(k_c), _ptr(v_c), kv_dtype, _ptr(ik_c), ik_dtype,
+                                    _ptr(ik_scale), _stream(stream)))
 
 
 def csa_sparse_attn_workspace_size(B, n_q, H, d, k):

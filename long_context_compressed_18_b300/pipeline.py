@@ -141,3 +141,57 @@ def run_layer(x: dict, s, ws: Workspace):
     if s.kind == "swa":
         return swa_layer(x, s)
     raise ValueError(s.kind)
+
+
+class DecodeState:
+    """Streaming CSA decode state of B sequences ("DeepSeek V4 技术解读" §2.1
+    applied one token at a time): compressed K/V and indexer-key caches of
+    capacity N_cap entries, the open block of raw tokens, and the per-sequence
+    token counts, all on the device.  ``append`` adds one token to every
+    sequence (closing and compressing a block every m tokens); ``select``
+    runs the Lightning Indexer and top-k for each sequence's new query at its
+    own position; ``attend`` is the sparse attention over the selection."""
+
+    def __init__(self, B: int, m: int, d: int, d_I: int, N_cap: int, x_dtype=torch.bfloat16,
+                 kv_dtype=torch.bfloat16, ik_kind: str = "e4m3", device="cuda"):
+        self.B, self.m, self.d, self.d_I, self.N_cap = B, m, d, d_I, N_cap
+        self.x_dtype, self.ik_kind = x_dtype, ik_kind
+        self.stage_logits = torch.zeros(B, m, dtype=torch.float32, device=device)
+        self.stage_k = torch.zeros(B, m, d, dtype=x_dtype, device=device)
+        self.stage_v = torch.zeros(B, m, d, dtype=x_dtype, device=device)
+        self.stage_ik = torch.zeros(B, m, d_I, dtype=x_dtype, device=device)
+        self.lens = torch.zeros(B, dtype=torch.int64, device=device)
+        self.k_c = torch.zeros(B, N_cap, d, dtype=kv_dtype, device=device)
+        self.v_c = torch.zeros(B, N_cap, d, dtype=kv_dtype, device=device)
+        if ik_kind == "e4m3":
+            self.ik_c = torch.zeros(B, N_cap, d_I, dtype=torch.uint8, device=device)
+            self.ik_scale = torch.ones(B, N_cap, dtype=torch.float32, device=device)
+        elif ik_kind == "e2m1":
+            self.ik_c = torch.zeros(B, N_cap, d_I // 2, dtype=torch.uint8, device=device)
+            self.ik_scale = torch.zeros(B, N_cap, d_I // 32, dtype=torch.uint8, device=device)
+        else:
+            self.ik_c = torch.zeros(B, N_cap, d_I, dtype=torch.float32 if ik_kind == "f32" else torch.bfloat16,
+                                    device=device)
+            self.ik_scale = None
+
+    def append(self, logit, k, v, ik):
+        """One token for every sequence: logit fp32 [B], k/v [B, d], ik [B, d_I]."""
+        lib.csa_decode_append(self.B, self.m, self.d, self.d_I, self.N_cap, logit, k, v, ik, _code(k),
+                              self.stage_logits, self.stage_k, self.stage_v, self.stage_ik, self.lens, self.k_c,
+                              self.v_c, _code(self.k_c), self.ik_c, _CODE[self.ik_kind], self.ik_scale)
+
+    def select(self, q_idx, q_dtype: str, q_scale, k: int, ws: Workspace, score_dtype: str = "f32",
+               head_weight=None, relu: bool = False):
+        """Top-k entries for the last n_q tokens of each sequence."""
+        B, n_q, H_I, d_I = q_idx.shape
+        topk = torch.empty(B, n_q, k, dtype=torch.int32, device=q_idx.device)
+        nbytes = lib.csa_index_topk_workspace_size(B, n_q, self.N_cap, H_I, d_I, k, _CODE[self.ik_kind],
+                                                   _CODE[score_dtype])
+        buf, nb = ws.get(nbytes)
+        lib.csa_index_topk_varlen(B, n_q, self.lens, self.m, self.N_cap, H_I, d_I, k, q_idx, _CODE[q_dtype], q_scale,
+                                  self.ik_c, _CODE[self.ik_kind], self.ik_scale, topk, buf, nb,
+                                  score_dtype=_CODE[score_dtype], head_weight=head_weight, relu=relu)
+        return topk
+
+    def attend(self, q, topk, scale: float, ws: Workspace, want_lse=True):
+        return sparse_attn(q, self.k_c, self.v_c, topk, scale, ws, want_lse)
