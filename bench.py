@@ -41,6 +41,9 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--batch", type=int, default=0, help="override the decode batch (profiling runs)")
+    p.add_argument("--idx-k", default="e4m3", choices=["e4m3", "e2m1"],
+                   help="decode indexer-key cache: E4M3 codes + row scale, or packed E2M1 + E4M3 block scales "
+                        "(widened inside the indexer)")
     p.add_argument("--scores", default="f32", choices=["f32", "bf16"],
                    help="index-score storage of the decode step (bf16: the pages' BF16 score variant)")
     return p.parse_args()
@@ -163,10 +166,9 @@ def _decode_shape(args, rank):
     return configs.Shape(**kw)
 
 
-def _oracle_queries(s, x, bs, entry_stride=1):
+def _oracle_queries(s, x, bs, entry_stride=1, k_kind="e4m3"):
     """The oracle's idx + top-k + attention for sequences ``bs`` (host copies),
     scoring every ``entry_stride``-th entry.  Returns seconds."""
-    import numpy as np
     import oracle
     t_total = 0.0
     for b in bs:
@@ -178,7 +180,7 @@ def _oracle_queries(s, x, bs, entry_stride=1):
         q = x["q"][b:b + 1].cpu()
         Nc = ik.shape[1]
         t0 = time.perf_counter()
-        _, _, sel = oracle.csa_index_topk(iq, iqs, "e4m3", ik, iks, "e4m3", Nc * s.m - 1, s.m, s.k)
+        _, _, sel = oracle.csa_index_topk(iq, iqs, "e4m3", ik, iks, k_kind, Nc * s.m - 1, s.m, s.k)
         oracle.attention(q, kc, vc, 1.0 / math.sqrt(s.d), oracle.SPARSE, idx=sel[None] * entry_stride)
         t_total += time.perf_counter() - t0
     return t_total
@@ -190,12 +192,25 @@ def run_decode(args, torch, dist, rank, world):
     dev = torch.cuda.current_device()
     s = _decode_shape(args, rank)
     B, Nc, k, HI, dI, H, d = s.B, s.N_c, s.k, s.H_I, s.d_I, s.H, s.d
-    x = inputs.make_inputs(s, device="cuda")
+    fp4 = args.idx_k == "e2m1"
+    if fp4:
+        # the FP4 cache as the compression epilogue stores it: N(0,1) keys
+        # through csa_compress at m = 1 (weight 1) into E2M1 + block scales
+        from long_context_compressed_18_b300 import configs, pipeline
+        s = configs.Shape(**{**s.__dict__, "idx_k_dtype": "bf16", "name": s.name.replace("_e4m3", "_e2m1keys")})
+        x = inputs.make_inputs(s, device="cuda")
+        (x["idx_k_c"], x["idx_k_c_scale"]), = pipeline.compress(
+            torch.zeros(B, Nc, device="cuda"), [x["idx_k_c"]], 1, ["e2m1"])
+        torch.cuda.synchronize()
+    else:
+        x = inputs.make_inputs(s, device="cuda")
+    kcode = lib.E2M1 if fp4 else lib.E4M3
+    in_gb = sum(t.numel() * t.element_size() for t in x.values() if t is not None) / 1e9
     topk = torch.empty(B, 1, k, dtype=torch.int32, device="cuda")
     out = torch.empty(B, 1, H, d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, 1, H, dtype=torch.float32, device="cuda")
     sdt = lib.BF16 if args.scores == "bf16" else lib.F32
-    ws_t_b = lib.csa_index_topk_workspace_size(B, 1, Nc, HI, dI, k, lib.E4M3, sdt)
+    ws_t_b = lib.csa_index_topk_workspace_size(B, 1, Nc, HI, dI, k, kcode, sdt)
     ws_a_b = lib.csa_sparse_attn_workspace_size(B, 1, H, d, k)
     ws_t = lib.empty_workspace(ws_t_b)
     ws_a = lib.empty_workspace(ws_a_b)
@@ -209,7 +224,7 @@ def run_decode(args, torch, dist, rank, world):
         if ev:
             ev[0].record(stream)
         lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, x["idx_q"], lib.E4M3, x["idx_q_scale"],
-                           x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], topk, ws_t, ws_t_b, score_dtype=sdt)
+                           x["idx_k_c"], kcode, x["idx_k_c_scale"], topk, ws_t, ws_t_b, score_dtype=sdt)
         if ev:
             ev[1].record(stream)
         lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, x["q"], x["k_c"], x["v_c"], lib.BF16, topk, out, lse,
@@ -317,7 +332,7 @@ def run_decode(args, torch, dist, rank, world):
             if used[j]:
                 stream.wait_event(down_done[j])           # step i-2's results have left these buffers
             lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, di["idx_q"], lib.E4M3, di["idx_q_scale"],
-                               x["idx_k_c"], lib.E4M3, x["idx_k_c_scale"], do["topk"], ws_t, ws_t_b, score_dtype=sdt)
+                               x["idx_k_c"], kcode, x["idx_k_c_scale"], do["topk"], ws_t, ws_t_b, score_dtype=sdt)
             lib.csa_sparse_attn(B, 1, H, d, Nc, k, tau, di["q"], x["k_c"], x["v_c"], lib.BF16, do["topk"],
                                 do["out"], do["lse"], ws_a, ws_a_b)
             comp_done[j].record(stream)
@@ -356,7 +371,7 @@ def run_decode(args, torch, dist, rank, world):
     alg = {  # algorithmic bytes per call: what the call must read and write at least
         # keys + row scales, the query and its head scales, the top-k indices
         # (the scores are an intermediate of the fused call)
-        "index_topk": B * (Nc * (dI + 4) + HI * (dI + 4) + k * 4),
+        "index_topk": B * (Nc * ((dI // 2 + dI // 32) if fp4 else (dI + 4)) + HI * (dI + 4) + k * 4),
         "sparse_attn": B * (k * d * 2 * 2 + H * d * 2 * 2 + k * 4 + H * 4),
     }
     achieved = alg[dom] / (avg[dom] / 1e3) / 1e9
@@ -370,10 +385,11 @@ def run_decode(args, torch, dist, rank, world):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        t1 = _oracle_queries(s, x, [0])
+        kk_kind = "e2m1" if fp4 else "e4m3"
+        t1 = _oracle_queries(s, x, [0], k_kind=kk_kind)
         nq = int(max(1, min(8, round(15.0 / max(t1, 1e-3)))))
         bs = [(7 * i) % B for i in range(nq)]
-        tt = _oracle_queries(s, x, bs)
+        tt = _oracle_queries(s, x, bs, k_kind=kk_kind)
         cpu = {"value": nq / tt, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{nq} of the 32 decode queries (full 262,144-entry caches), {tt:.1f} s"}
 
@@ -384,12 +400,14 @@ def run_decode(args, torch, dist, rank, world):
     res = {
         "metric": METRIC, "value": _job_rate(world, B * K, ms), "unit": "queries/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (indexer) / bf16 (attention)",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3 x e2m1->e4m3" if fp4 else "e4m3") + " (indexer) / bf16 (attention)",
         "data": "synthetic",
         "config": {"workload": s.name, "batch_per_gpu": B, "ctx_tokens": s.n, "compressed_entries": Nc,
-                   "indexer": f"{HI}x{dI} e4m3", "index_scores": args.scores, "top_k": k,
+                   "indexer": f"{HI}x{dI} e4m3" + (", e2m1 key cache" if fp4 else ""),
+                   "index_scores": args.scores, "top_k": k,
                    "attention": f"{H}x{d} bf16",
-                   "l2": "inputs (5.2 GB per GPU) exceed L2; no flush",
+                   "l2": f"inputs ({in_gb:.1f} GB per GPU) exceed L2; no flush",
                    "launch": "one step (indexer with fused top-k collection, select, sparse attention) captured "
                              "in a CUDA graph and replayed",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},

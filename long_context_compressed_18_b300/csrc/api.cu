@@ -64,7 +64,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // 2D row-major [rows, inner] tensor, 128-byte swizzled boxes of
 // [box_rows, box_inner] (box_inner * element size = 128 bytes).
 csa_status_t make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, uint64_t inner,
-                      uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows)
+                      uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(CSA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -73,7 +74,7 @@ csa_status_t make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(CSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return CSA_OK;
@@ -148,7 +149,11 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, QPos q_pos0, 
     const bool fp8 = q_dtype == CSA_E4M3;
     const void* keys = k_idx;
     const float* ksc = reinterpret_cast<const float*>(k_scale);
-    if (k_dtype == CSA_E2M1) {
+    const int T = indexer_group_tokens(n_q_rows);
+    // decode groups widen FP4 keys inside the indexer; prefill groups, which
+    // read every key tile many times, widen once into the workspace
+    const bool kfp4 = k_dtype == CSA_E2M1 && T == 1;
+    if (k_dtype == CSA_E2M1 && !kfp4) {
         uint8_t* x8 = reinterpret_cast<uint8_t*>(ws);
         float* S = reinterpret_cast<float*>(x8 + align_up((size_t)B * N_c * d_I, 256));
         csa_status_t st = cuda_status(
@@ -159,7 +164,6 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, QPos q_pos0, 
         keys = x8;
         ksc = S;
     }
-    const int T = indexer_group_tokens(n_q_rows);
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint32_t elem = fp8 ? 1 : 2;
     const uint32_t box_inner = 128 / elem;
@@ -167,11 +171,15 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, QPos q_pos0, 
     csa_status_t st = make_map(&tq, q_idx, dt, (uint64_t)d_I, (uint64_t)B * n_q * H_I, (uint64_t)d_I * elem, box_inner,
                                (uint32_t)indexer_box_rows(T));
     if (st != CSA_OK) return st;
-    st = make_map(&tk, keys, dt, (uint64_t)d_I, (uint64_t)B * N_c, (uint64_t)d_I * elem, box_inner, 128);
+    if (kfp4)   // packed rows of d_I / 2 bytes, copied unswizzled for the converter warps
+        st = make_map(&tk, keys, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)d_I / 2, (uint64_t)B * N_c, (uint64_t)d_I / 2,
+                      (uint32_t)d_I / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    else
+        st = make_map(&tk, keys, dt, (uint64_t)d_I, (uint64_t)B * N_c, (uint64_t)d_I * elem, box_inner, 128);
     if (st != CSA_OK) return st;
     return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, head_w, relu, ksc, scores, sbf16, B, n_q, i_start,
                                          n_q_rows,
-                                         q_pos0, m, N_c, num_sms(), wmax, wmax_ld, s),
+                                         q_pos0, m, N_c, num_sms(), wmax, wmax_ld, kfp4, s),
                        "indexer_tc launch");
 }
 

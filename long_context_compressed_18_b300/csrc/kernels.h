@@ -106,7 +106,7 @@ cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUte
                               const float* q_scale, const float* head_w, bool relu, const float* k_scale,
                               void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, QPos q_pos0, int m, int Nc,
-                              int num_sms, uint32_t* wmax, int wmax_ld, cudaStream_t s);
+                              int num_sms, uint32_t* wmax, int wmax_ld, bool kfp4, cudaStream_t s);
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* head_w, bool relu,
                                const float* k, const float* k_scale, void* scores, bool score_bf16, int B,
                                int n_q_total, int i_start, int n_q_rows,

@@ -240,7 +240,8 @@ def test_index_topk_varlen_equals_uniform_route():
 
 # ---- a short streaming decode loop ----------------------------------------------------
 
-def test_streaming_decode_loop_stagewise():
+@pytest.mark.parametrize("ik_kind", ["e4m3", "e2m1"])
+def test_streaming_decode_loop_stagewise(ik_kind):
     """Sequences of different lengths grow token by token; after each
     append every sequence's new query selects among its closed entries and
     attends to them.  Each stage is checked against the oracle on the same
@@ -257,13 +258,13 @@ def test_streaming_decode_loop_stagewise():
     K = (torch.randn(B, nmax, d, generator=g) * d ** -0.25).to(torch.bfloat16)
     V = torch.randn(B, nmax, d, generator=g).to(torch.bfloat16)
     IK = torch.randn(B, nmax, dI, generator=g).to(torch.bfloat16)
-    st = pipeline.DecodeState(B, m, d, dI, N_cap, ik_kind="e4m3")
+    st = pipeline.DecodeState(B, m, d, dI, N_cap, ik_kind=ik_kind)
     # the prefix: its closed blocks through the compression kernel, the open block staged
     for b, l in enumerate(L0):
         nc = l // m
         (kc, _), (vc, _), (ikc, iks) = pipeline.compress(lg[b:b + 1, :nc * m].to(DEV),
                                                          [K[b:b + 1, :nc * m].to(DEV), V[b:b + 1, :nc * m].to(DEV),
-                                                          IK[b:b + 1, :nc * m].to(DEV)], m, ["bf16", "bf16", "e4m3"])
+                                                          IK[b:b + 1, :nc * m].to(DEV)], m, ["bf16", "bf16", ik_kind])
         st.k_c[b, :nc], st.v_c[b, :nc], st.ik_c[b, :nc], st.ik_scale[b, :nc] = kc[0], vc[0], ikc[0], iks[0]
         o = nc * m
         st.stage_logits[b, :l - o] = lg[b, o:l].to(DEV)
@@ -294,7 +295,7 @@ def test_streaming_decode_loop_stagewise():
             assert np.all(np.abs(gk - want_k) <= 2.0 ** -8 * np.abs(want_k) + 1e-5), b
             # stage 2: selection over the GPU-written keys
             s64, _, want_sel = oracle.csa_index_topk(q_idx[b:b + 1], q_s[b:b + 1], "e4m3", ikc[b:b + 1],
-                                                     iks[b:b + 1], "e4m3", nb - 1, m, k)
+                                                     iks[b:b + 1], ik_kind, nb - 1, m, k)
             topk_near_tie_check(sel[b], want_sel, s64, [min(nb // m, N_cap)], k)
         # stage 3: attention on the GPU's selection over the GPU-written caches
         kc_h, vc_h = host(st.k_c).float(), host(st.v_c).float()

@@ -54,6 +54,8 @@ INDEX_CASES = [
     dict(B=3, n_q=1, q_pos0=4 * 6000 - 1, m=4, Nc=6000, HI=64, dI=128, q_dt="e4m3", k_dt="e4m3"),
     dict(B=1, n_q=65, q_pos0=1000, m=4, Nc=400, HI=64, dI=128, q_dt="e4m3", k_dt="e4m3"),
     dict(B=2, n_q=9, q_pos0=2000, m=4, Nc=700, HI=64, dI=128, q_dt="e4m3", k_dt="e2m1"),
+    dict(B=3, n_q=1, q_pos0=4 * 6001 - 1, m=4, Nc=6001, HI=64, dI=128, q_dt="e4m3", k_dt="e2m1"),   # widened in-kernel
+    dict(B=2, n_q=3, q_pos0=4 * 2000 - 3, m=4, Nc=2000, HI=64, dI=128, q_dt="e4m3", k_dt="e2m1"),
     dict(B=2, n_q=1, q_pos0=4 * 3000 - 1, m=4, Nc=3000, HI=64, dI=128, q_dt="bf16", k_dt="bf16"),
 ]
 
