@@ -36,7 +36,8 @@
 // (about 1.8x the rate of TMA tile::gather4 from two warps on an L2-resident
 // table: 23.7 vs 12.9 bytes per cycle per SM, measured on B300); each gather
 // warp publishes tile j after issuing tile j+1, once its own copies of tile j
-// have landed (cp.async.wait_group, then a proxy fence, then its arrival).
+// have landed (cp.async.wait_group, then a proxy fence, then its arrival) --
+// or at once, before blocking on the ring, when no stage is free for tile j+1.
 //   warps 0-3  softmax and epilogue, two passes over 32-column chunks of S
 //              (row maximum, then exponentials) so that they fit the 128
 //              registers a thread of a 512-thread CTA has;
@@ -241,9 +242,22 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
                 }
             };
             bool ok = true;
+            int published = 0;                 // tiles this warp has published
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % STAGES;
                 const uint32_t par = ((j / STAGES) & 1) ^ 1;
+                if (published < j) {
+                    // tile j-1 is still unpublished: if the ring has no free
+                    // stage for tile j yet, publish j-1 first rather than hold
+                    // it behind the wait (the consumers free the stage)
+                    int ready = 1;
+                    if (lane == 0) ready = mbar_try_wait(&k_empty[st], par) && mbar_try_wait(&v_empty[st], par);
+                    if (!__shfl_sync(FULL, ready, 0)) {
+                        cp_async_wait<0>();
+                        publish(j - 1);
+                        published = j;
+                    }
+                }
                 int w = 1;
                 if (lane == 0) w = mbar_wait(&k_empty[st], par, abort_flag);
                 if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
@@ -251,9 +265,10 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
                 if (lane == 0) w = mbar_wait(&v_empty[st], par, abort_flag);
                 if (!__shfl_sync(FULL, w, 0)) { ok = false; break; }
                 gather(p.v_rows, sV + st * V_BYTES, j);
-                if (j >= 1) {
+                if (published < j) {
                     cp_async_wait<2>();        // tile j-1's two groups have landed
                     publish(j - 1);
+                    published = j;
                 }
             }
             cp_async_wait<0>();                // nothing of this warp is left in flight
@@ -423,14 +438,15 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
                         tc_fence_after();
                         const float f = (move && m_ref != -INFINITY) ? ex2_approx(m_ref - m_new) : 1.f;
                         const uint32_t o_addr = tmem + lane_base + O_COL;
+                        // 16 columns at a time: the tile's scores stay live meanwhile
 #pragma unroll
-                        for (int q = 0; q < D / 32; ++q) {
-                            uint32_t ov[32];
-                            tmem_ld32(o_addr + 32 * q, ov);
+                        for (int q = 0; q < D / 16; ++q) {
+                            uint32_t ov[16];
+                            tmem_ld16(o_addr + 16 * q, ov);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
-                            tmem_st32(o_addr + 32 * q, ov);
+                            for (int u = 0; u < 16; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * f);
+                            tmem_st16(o_addr + 16 * q, ov);
                         }
                         l_run *= f;
                     }

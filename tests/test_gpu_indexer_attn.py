@@ -125,6 +125,10 @@ SPARSE_CASES = [
     dict(B=1, n_q=20, q_pos0=4 * 3000 - 20, m=4, N_c=3000, k=1024, H=64, d=128, dt="bf16"),
     # ragged last tile (k = 200) with early queries that see few or no entries
     dict(B=1, n_q=40, q_pos0=0, m=4, N_c=100, k=200, H=64, d=128, dt="bf16"),
+    # more query tokens than SMs, full sets of eight tiles; then from the start
+    # of the context, so tokens with no, one or a few tiles follow one another
+    dict(B=2, n_q=400, q_pos0=4 * 3000 - 400, m=4, N_c=3000, k=1024, H=64, d=128, dt="bf16"),
+    dict(B=1, n_q=700, q_pos0=0, m=4, N_c=700, k=512, H=64, d=128, dt="bf16"),
     dict(B=1, n_q=100, q_pos0=0, m=4, N_c=256, k=64, H=8, d=64, dt="f32"),                  # short sets, -1 pads
     dict(B=2, n_q=2, q_pos0=300, m=1, N_c=301, k=200, H=32, d=64, dt="f32"),
 ]
