@@ -16,6 +16,7 @@
 // them in split order, so results are deterministic.
 #include "common.cuh"
 #include "kernels.h"
+#include "attn_merge.cuh"
 
 namespace csa {
 
@@ -199,72 +200,14 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
     }
 }
 
-// Merge split partials in split order: M = max m_s, L = sum l_s 2^(m_s - M),
-// o = sum o_s 2^(m_s - M) / L.  One thread per (row, head, 8 channels).
+// Merge split partials (attn_merge.cuh).  One thread per (row, head, 8 channels).
 template <typename TIO>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgsT<TIO> a, int H, int D)
 {
     const long long n = (long long)a.B * a.n_q * H * (D / 8);
     const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (x >= n) return;
-    const long long rh = x / (D / 8);        // row * H + h
-    const int c = (int)(x % (D / 8)) * 8;
-    const long long stride = (long long)a.B * a.n_q * H;
-    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);   // (m, l) per split and row
-    // Splits are merged in split order, SU at a time with all their loads in
-    // flight: every split of a batch is weighted against the running maximum
-    // M (the batch's maximum folded in first; earlier sums rescaled).  Up to
-    // SU splits this is exactly o = sum_s w_s o_s, L = sum_s w_s l_s with
-    // w_s = 2^(m_s - max_s m_s).
-    constexpr int SU = 8;
-    float M = -INFINITY, L = 0.f, o[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) o[u] = 0.f;
-    for (int s0 = 0; s0 < a.n_splits; s0 += SU) {
-        float2 mv[SU];
-        float4 pa[SU], pb[SU];
-#pragma unroll
-        for (int u = 0; u < SU; ++u) {
-            const int sp = s0 + u;
-            if (sp < a.n_splits) {
-                const long long r = sp * stride + rh;
-                mv[u] = ml[r];
-                const float4* po = reinterpret_cast<const float4*>(a.part_o + r * D + c);
-                pa[u] = po[0];
-                pb[u] = po[1];
-            } else {
-                mv[u] = make_float2(-INFINITY, 0.f);
-                pa[u] = pb[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        float Mb = M;
-#pragma unroll
-        for (int u = 0; u < SU; ++u) Mb = fmaxf(Mb, mv[u].x);
-        if (Mb == -INFINITY) continue;            // every split so far is empty
-        const float rs = exp2f(M - Mb);           // 0 while M = -inf
-        L *= rs;
-#pragma unroll
-        for (int v = 0; v < 8; ++v) o[v] *= rs;
-#pragma unroll
-        for (int u = 0; u < SU; ++u) {
-            const float w = exp2f(mv[u].x - Mb);  // 0 for empty splits (m = -inf)
-            L = fmaf(mv[u].y, w, L);
-            o[0] = fmaf(pa[u].x, w, o[0]);
-            o[1] = fmaf(pa[u].y, w, o[1]);
-            o[2] = fmaf(pa[u].z, w, o[2]);
-            o[3] = fmaf(pa[u].w, w, o[3]);
-            o[4] = fmaf(pb[u].x, w, o[4]);
-            o[5] = fmaf(pb[u].y, w, o[5]);
-            o[6] = fmaf(pb[u].z, w, o[6]);
-            o[7] = fmaf(pb[u].w, w, o[7]);
-        }
-        M = Mb;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) o[u] *= inv;
-    Vec8<TIO>::store(a.out + rh * D + c, o);
-    if (a.lse && c == 0) a.lse[rh] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    merge_split_partials(a, H, D, x / (D / 8), (int)(x % (D / 8)) * 8);
 }
 
 size_t attn_smem_bytes(int H, int D)
