@@ -432,6 +432,61 @@ def _pairs(s, window_or_k=None):
     return sum(nv)
 
 
+def _oracle_prefill_layer(s, x, budget_s):
+    """The oracle on one prefill layer: the compression of every token, then
+    stratified query rows (evenly spread over the call's rows, so short and
+    long key sets are both sampled) through scores, top-k and attention.
+    Returns (seconds for the whole layer, extrapolated from the rows; the
+    sample's description)."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    f32 = lambda t: np.ascontiguousarray(t.float().numpy())
+    tau = 1.0 / math.sqrt(s.d)
+    q = x["q"]
+    if s.kind in ("csa", "hca"):
+        lg = f32(x["logits"])
+        Kc = oracle.compress(lg, f32(x["k"]), s.m).astype(np.float32)
+        Vc = oracle.compress(lg, f32(x["v"]), s.m).astype(np.float32)
+    if s.kind == "csa":
+        ic = oracle.compress(lg, f32(x["idx_k"]), s.m).astype(np.float32)
+        if s.idx_k_dtype == "e4m3":
+            ik, iks = oracle.quant_e4m3_rows(ic)
+        elif s.idx_k_dtype == "e2m1":
+            ik, iks = oracle.quant_e2m1_blocks(ic)
+        else:
+            ik, iks = ic, None
+    if s.kind == "swa":
+        Kr, Vr = f32(x["k"]), f32(x["v"])
+    t_comp = time.perf_counter() - t0
+
+    def row(f):
+        b, i = divmod(int(f), s.n_q)
+        qr = q[b:b + 1, i:i + 1]
+        if s.kind == "csa":
+            _, _, sel = oracle.csa_index_topk(x["idx_q"], x["idx_q_scale"], s.idx_q_dtype, ik, iks, s.idx_k_dtype,
+                                              s.q_pos0, s.m, s.k, rows=np.array([f]))
+            oracle.attention(qr, Kc[b:b + 1], Vc[b:b + 1], tau, oracle.SPARSE, idx=sel[None])
+        elif s.kind == "hca":
+            oracle.attention(qr, Kc[b:b + 1], Vc[b:b + 1], tau, oracle.CLOSED_BLOCKS, q_pos0=s.q_pos0 + i, m=s.m)
+        else:
+            oracle.attention(qr, Kr[b:b + 1], Vr[b:b + 1], tau, oracle.WINDOW, q_pos0=s.q_pos0 + i, window=s.window)
+
+    rows_total = s.B * s.n_q
+    t1 = time.perf_counter()
+    row(rows_total - 1)                     # the longest key set: sizes the sample
+    t_one = time.perf_counter() - t1
+    R = int(max(4, min(64, budget_s / max(t_one, 1e-4))))
+    picks = np.unique(np.linspace(0, rows_total - 1, R).round().astype(np.int64))
+    t1 = time.perf_counter()
+    for f in picks:
+        row(f)
+    t_rows = time.perf_counter() - t1
+    est = t_comp + t_rows / picks.size * rows_total
+    return est, (f"{s.name}: compression of all {s.B * s.n} tokens ({t_comp:.1f} s) + {picks.size} of {rows_total} "
+                 f"query rows evenly spaced ({t_rows:.1f} s), the row time extrapolated to every row")
+
+
 def run_config(args, torch, name):
     """Per-stage CUDA-event timing of a prefill workload (one rank): every
     kernel of each layer is timed on its own, with its roofline fraction."""
@@ -554,10 +609,23 @@ def run_config(args, torch, name):
             torch.cuda.empty_cache()
     tot = sum(v["ms"] for st in stages_all.values() for v in st.values())
     n_q = sum(s.B * s.n_q for s in layers)
+    # ---- cpu baseline: the oracle on a bounded, stratified sample of each layer ----
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        est, samples = 0.0, []
+        for s in layers:
+            xh = {kk: (None if v is None else v.cpu()) for kk, v in inputs.make_inputs(s, device="cuda").items()}
+            t_layer, desc = _oracle_prefill_layer(s, xh, budget_s=24.0 / len(layers))
+            est += t_layer
+            samples.append(desc)
+            del xh
+        cpu = {"value": n_q / est, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": "; ".join(samples), "extrapolated": True}
     return {"metric": "prefill queries/s (all stages of the workload)", "value": n_q / (tot / 1e3),
             "unit": "queries/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot,
             "higher_is_better": True, "config": {"workload": name}, "stages": stages_all,
-            "peak_source": peak_src, "clocks": clk.summary(), "data": "synthetic"}
+            "peak_source": peak_src, "clocks": clk.summary(), "data": "synthetic", "cpu_baseline": cpu}
 
 
 def run_reference(args, torch, rank, world):
