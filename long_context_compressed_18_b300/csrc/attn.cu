@@ -26,6 +26,7 @@ constexpr int ATT_KT = 32;   // keys per tile
 template <typename TIO, int H, int D>
 __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a)
 {
+    grid_dep_entry();
     constexpr int TPH = ATT_THREADS / H;   // threads per head
     constexpr int KPT = ATT_KT / TPH;      // keys per thread per tile
     constexpr int CPT = D / TPH;           // output channels per thread
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attn_simt_kernel(AttnArgsT<TIO> a
 template <typename TIO>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgsT<TIO> a, int H, int D)
 {
+    grid_dep_entry();
     const long long n = (long long)a.B * a.n_q * H * (D / 8);
     const long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (x >= n) return;
@@ -222,11 +224,11 @@ static cudaError_t launch_h(const AttnArgsT<TIO>& a, cudaStream_t s)
     const size_t smem = attn_smem_bytes(H, D);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(a.n_q * a.n_splits, a.B, a.H_kv);
-    kern<<<grid, ATT_THREADS, smem, s>>>(a);
+    (void)launch_pdl(kern, dim3(grid), dim3(ATT_THREADS), smem, s, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.n_splits == 1) return e;
     const long long n = (long long)a.B * a.n_q * a.H_tot * (D / 8);
-    attn_combine_kernel<TIO><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, a.H_tot, D);
+    (void)launch_pdl(attn_combine_kernel<TIO>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, a, a.H_tot, D);
     return cudaGetLastError();
 }
 
@@ -234,7 +236,7 @@ cudaError_t launch_attn_combine(const AttnArgsT<__nv_bfloat16>& a, int H, int D,
 {
     const long long n = (long long)a.B * a.n_q * H * (D / 8);
     if (n == 0) return cudaSuccess;
-    attn_combine_kernel<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, H, D);
+    (void)launch_pdl(attn_combine_kernel<__nv_bfloat16>, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, a, H, D);
     return cudaGetLastError();
 }
 

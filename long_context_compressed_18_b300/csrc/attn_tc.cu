@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v, const AttnTcParams p)
 {
+    grid_dep_entry();
     using namespace atc;
     using C = Cfg<MODE, STAGES, QROWS>;
     using R = Roles<MODE>;
@@ -619,7 +620,7 @@ static void launch_one(dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk, 
     auto kern = attn_tc_kernel<MODE, STAGES, QROWS>;
     constexpr int smem = atc::Cfg<MODE, STAGES, QROWS>::SMEM;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    kern<<<grid, atc::Roles<MODE>::THREADS, smem, s>>>(tq, tk, tv, p);
+    (void)launch_pdl(kern, dim3(grid), dim3(atc::Roles<MODE>::THREADS), smem, s, tq, tk, tv, p);
 }
 
 cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

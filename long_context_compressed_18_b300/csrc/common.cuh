@@ -37,6 +37,40 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with launch_pdl, so the next kernel in the stream may be scheduled while
+// this one still runs; each kernel therefore opens with grid_dep_entry()
+// before it touches global memory: it waits until the grid before it in the
+// stream has completed with its writes visible (and, since that grid waited
+// the same way, every earlier one too), then allows the next grid to launch.
+// The next grid's CTAs then occupy free SM slots and wait at their own entry,
+// which hides its launch latency and ramp behind this grid's tail.  A kernel
+// launched without the attribute passes the wait at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_entry()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)

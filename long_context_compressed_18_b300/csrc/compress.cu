@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(int B, int n, int m, i
                                                        const Tin* __restrict__ x, void* out,
                                                        void* out_scale)
 {
+    grid_dep_entry();
     __shared__ float4 red[256][2];
     const int G = d >> 3;  // threads per output row (power of two, <= 32)
     const int TP = 256 / P, tid = threadIdx.x;
@@ -164,8 +165,8 @@ cudaError_t launch_compress(int B, int n, int m, int d, const float* logits, con
     const long long rows_per_cta = bs / P / G;
     const unsigned grid = (unsigned)((B * (long long)Nc + rows_per_cta - 1) / rows_per_cta);
 #define CSA_LAUNCH_COMPRESS(TIN, OK)                                                       \
-    compress_kernel<TIN, OK><<<grid, bs, 0, s>>>(B, n, m, Nc, d, P, logits,                \
-                                                 reinterpret_cast<const TIN*>(x), out, out_scale)
+    (void)launch_pdl(compress_kernel<TIN, OK>, dim3(grid), dim3(bs), 0, s, B, n, m, Nc, d, P, logits,    \
+                     reinterpret_cast<const TIN*>(x), out, out_scale)
     if (x_bf16) {
         switch (out_kind) {
             case 0: CSA_LAUNCH_COMPRESS(__nv_bfloat16, 0); break;
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(256, 4) compress_channel_kernel(int B, int n, 
                                                                const Tin* __restrict__ x, void* out,
                                                                void* out_scale)
 {
+    grid_dep_entry();
     const int G = d >> 3;   // threads per output row (power of two, <= 32)
     const long long rows = (long long)B * Nc;
     const long long row = (long long)blockIdx.x * (256 / G) + threadIdx.x / G;
@@ -246,8 +248,8 @@ cudaError_t launch_compress_per_channel(int B, int n, int m, int d, const float*
     const int rows_per_cta = 256 / (d / 8);
     const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
 #define CSA_LAUNCH_CHANNEL(TIN, OK)                                                                  \
-    compress_channel_kernel<TIN, OK><<<grid, 256, 0, s>>>(B, n, m, Nc, d, logits,                    \
-                                                          reinterpret_cast<const TIN*>(x), out, out_scale)
+    (void)launch_pdl(compress_channel_kernel<TIN, OK>, dim3(grid), dim3(256), 0, s, B, n, m, Nc, d, logits,   \
+                     reinterpret_cast<const TIN*>(x), out, out_scale)
     if (x_bf16) {
         switch (out_kind) {
             case 0: CSA_LAUNCH_CHANNEL(__nv_bfloat16, 0); break;
@@ -348,6 +350,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 __global__ void __launch_bounds__(cmpt::THREADS, cmpt::CTAS_PER_SM)
 compress_tile_kernel(const __grid_constant__ CompressTileParams p)
 {
+    grid_dep_entry();
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ uint64_t full[cmpt::MAX_STAGES], empty[cmpt::MAX_STAGES];
     __shared__ float wts[2][cmpt::MAX_R * cmpt::MAX_M];   // by tile parity
@@ -524,7 +527,7 @@ cudaError_t launch_compress_tiles(int B, int n, int m, int n_streams, const floa
     cudaError_t e = cudaFuncSetAttribute(compress_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(n_tiles < slots ? n_tiles : slots);
-    compress_tile_kernel<<<grid, cmpt::THREADS, smem, s>>>(p);
+    (void)launch_pdl(compress_tile_kernel, dim3(grid), dim3(cmpt::THREADS), smem, s, p);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 template <typename TIN>
 __global__ void __launch_bounds__(APPEND_THREADS) decode_append_kernel(DecodeAppendArgs a)
 {
+    grid_dep_entry();
     __shared__ float w[DECODE_MAX_M];
     __shared__ float row[256];
     __shared__ float red[APPEND_THREADS / 32];
@@ -142,8 +143,8 @@ __global__ void __launch_bounds__(APPEND_THREADS) decode_append_kernel(DecodeApp
 cudaError_t launch_decode_append(const DecodeAppendArgs& a, bool x_bf16, cudaStream_t s)
 {
     if (a.B == 0) return cudaSuccess;
-    if (x_bf16) decode_append_kernel<__nv_bfloat16><<<a.B, APPEND_THREADS, 0, s>>>(a);
-    else decode_append_kernel<float><<<a.B, APPEND_THREADS, 0, s>>>(a);
+    if (x_bf16) (void)launch_pdl(decode_append_kernel<__nv_bfloat16>, dim3(a.B), dim3(APPEND_THREADS), 0, s, a);
+    else (void)launch_pdl(decode_append_kernel<float>, dim3(a.B), dim3(APPEND_THREADS), 0, s, a);
     return cudaGetLastError();
 }
 

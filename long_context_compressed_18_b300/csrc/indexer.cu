@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(idx::threads<T, KFP4>(), KFP4 ? 2 : 1) indexer
     void* __restrict__ scores, int score_bf16, int n_q_total, int i_start, int n_q_rows, QPos qp, int m,
     int Nc, int n_splits, int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
 {
+    grid_dep_entry();
     using C = idx::Cfg<FP8, T, KFP4>;
     static_assert(!WMAX || T == 1, "warp maxima: decode groups");
     extern __shared__ uint8_t smem_raw[];
@@ -489,6 +490,7 @@ __global__ void __launch_bounds__(256) indexer_f32_kernel(
     const float* __restrict__ k, const float* __restrict__ k_scale, void* __restrict__ scores, int score_bf16,
     int n_q_total, int i_start, int n_q_rows, QPos qp, int m, int Nc, int HI, int dI)
 {
+    grid_dep_entry();
     extern __shared__ float qs[];
     const int r = blockIdx.y;          // chunk-local row = b * n_q_rows + i
     const int b = r / n_q_rows, i = r % n_q_rows;
@@ -525,6 +527,7 @@ __global__ void __launch_bounds__(256) fp4_to_e4m3_kernel(const uint8_t* __restr
                                                           uint8_t* __restrict__ x8, float* __restrict__ S,
                                                           long long rows, int d)
 {
+    grid_dep_entry();
     const int nb = d / 32;
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= rows * nb) return;
@@ -562,7 +565,7 @@ cudaError_t launch_fp4_to_e4m3(const uint8_t* packed, const uint8_t* sc, uint8_t
 {
     const long long n = rows * (d / 32);
     if (n == 0) return cudaSuccess;
-    fp4_to_e4m3_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(packed, sc, x8, S, rows, d);
+    (void)launch_pdl(fp4_to_e4m3_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, packed, sc, x8, S, rows, d);
     return cudaGetLastError();
 }
 
@@ -576,9 +579,7 @@ cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float
     size_t smem = (size_t)(HI * dI + HI) * sizeof(float);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(indexer_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    indexer_f32_kernel<<<grid, 256, smem, s>>>(q, q_scale, head_w, relu ? 1 : 0, k, k_scale, scores,
-                                               score_bf16 ? 1 : 0, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, HI,
-                                               dI);
+    (void)launch_pdl(indexer_f32_kernel, dim3(grid), dim3(256), smem, s, q, q_scale, head_w, relu ? 1 : 0, k, k_scale, scores, score_bf16 ? 1 : 0, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, HI, dI);
     return cudaGetLastError();
 }
 
@@ -605,9 +606,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     auto kern = indexer_tc_kernel<FP8, T, WMAX, KFP4>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     dim3 grid(n_groups * splits, B);
-    kern<<<grid, idx::threads<T, KFP4>(), C::SMEM, s>>>(tq, tk, q_scale, head_w, relu ? 1 : 0, k_scale, scores,
-                                             score_bf16 ? 1 : 0, n_q_total,
-                                             i_start, n_q_rows, q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
+    (void)launch_pdl(kern, dim3(grid), dim3(idx::threads<T, KFP4>()), C::SMEM, s, tq, tk, q_scale, head_w, relu ? 1 : 0, k_scale, scores, score_bf16 ? 1 : 0, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
     return cudaGetLastError();
 }
 

@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_smem_kernel(
     const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc,
     int k, int32_t* __restrict__ out, long long out_b_stride)
 {
+    grid_dep_entry();
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw);
@@ -577,26 +578,50 @@ __device__ void collect_entries(const ST* __restrict__ row, int c0, int len, uin
 }
 
 // Collection threshold from the row's warp maxima (wmax: the largest score
-// key of each run of 32 consecutive entries, written by the indexer): the
-// exact kk-th largest of the nw = ceil(L / 32) maxima.  Those kk maxima are
-// distinct entries, so at least kk entries have a key at or above it: every
-// entry of the row's top kk does, and collecting key >= it is complete.  With
-// fewer maxima than kk, 0 (take every entry).  keys: shared buffer of nw keys.
+// key of each run of 32 consecutive entries, written by the indexer): a key
+// at or below the kk-th largest of the nw = ceil(L / 32) maxima.  Those kk
+// maxima are distinct entries, so at least kk entries have a key at or above
+// it: every entry of the row's top kk does, and collecting key >= it is
+// complete.  One histogram level suffices: the maxima crowd into a narrow
+// key range, so they are spread first as (key - lo) << s (s putting the top
+// bit of hi - lo at bit 31), and the returned key is the lower edge of the
+// 2,048-bin level's bin holding rank kk (at most one bin, span / 2048, below
+// the exact value).  With fewer maxima than kk, 0 (take every entry).
+// keys: shared buffer of nw keys.
 __device__ uint32_t wmax_threshold(const uint32_t* __restrict__ wrow, int nw, int kk, uint32_t* keys, TopkShared& sh)
 {
     if (nw < kk) return 0u;
+    const int tid = threadIdx.x;
     clear_hist(sh, 2048);
-    __syncthreads();
-    for (int x = threadIdx.x; x < nw; x += TOPK_THREADS) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int x = tid; x < nw; x += TOPK_THREADS) {
         const uint32_t key = __ldcg(wrow + x);
         keys[x] = key;
-        atomicAdd(&sh.hist[key >> 21], 1u);
+        lo = min(lo, key);
+        hi = max(hi, key);
+    }
+#pragma unroll
+    for (int dd = 16; dd > 0; dd >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
+    }
+    if ((tid & 31) == 0) {
+        sh.scan[tid >> 5] = lo;
+        sh.warp_take[tid >> 5] = hi;
     }
     __syncthreads();
-    uint32_t T;
-    int teq;
-    radix_threshold(keys, nw, kk, sh, T, teq);
-    return T;
+    lo = 0xFFFFFFFFu;
+    hi = 0u;
+    for (int q = 0; q < TOPK_WARPS; ++q) {
+        lo = min(lo, sh.scan[q]);
+        hi = max(hi, sh.warp_take[q]);
+    }
+    const uint32_t span = hi - lo;
+    const int shl = span ? __clz(span) : 0;
+    for (int x = tid; x < nw; x += TOPK_THREADS) atomicAdd(&sh.hist[((keys[x] - lo) << shl) >> 21], 1u);
+    __syncthreads();
+    find_bin<2048>(sh, (uint32_t)kk);
+    return lo + ((sh.bin << 21) >> shl);
 }
 
 template <typename ST>
@@ -604,6 +629,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
     const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k,
     int n_chunks, LongRowWs w, const uint32_t* __restrict__ wmax, int wmax_ld)
 {
+    grid_dep_entry();
     // the chunk's entries go to a shared-memory list, then one global atomic
     // reserves the chunk's slice of the row's list (whose order does not
     // matter to the select kernel)
@@ -847,6 +873,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k,
     LongRowWs w, int fast_ok, int32_t* __restrict__ out, long long out_b_stride)
 {
+    grid_dep_entry();
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
     const int r = blockIdx.x;
@@ -918,6 +945,7 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
     const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k, int cap,
     int32_t* __restrict__ out, long long out_b_stride)
 {
+    grid_dep_entry();
     extern __shared__ __align__(16) uint8_t smem_raw[];
     __shared__ TopkShared sh;
     __shared__ uint32_t n_cnt;
@@ -994,7 +1022,7 @@ static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, Q
     if (!fast_ok) smem = 0;
     auto kern = topk_lr_select_kernel<ST>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok, out, out_b_stride);
+    (void)launch_pdl(kern, dim3(rows), dim3(TOPK_THREADS), smem, s, scores, ld, n_q_rows, q_pos0, m, N_c, k, w, fast_ok, out, out_b_stride);
     return cudaGetLastError();
 }
 
@@ -1012,15 +1040,14 @@ static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_
         const size_t smem = (size_t)(N_c > 0 ? N_c : 1) * sizeof(uint32_t);
         auto kern = topk_smem_kernel<ST>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
+        (void)launch_pdl(kern, dim3(rows), dim3(TOPK_THREADS), smem, s, scores, ld, n_q_rows, q_pos0, m, N_c, k, out, out_b_stride);
         return cudaGetLastError();
     }
     if (p.n_chunks == 1) {
         const size_t smem = row_smem_bytes(N_c, k);
         auto kern = topk_kernel<ST>;
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        kern<<<rows, TOPK_THREADS, smem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, row_cap(N_c, k), out,
-                                              out_b_stride);
+        (void)launch_pdl(kern, dim3(rows), dim3(TOPK_THREADS), smem, s, scores, ld, n_q_rows, q_pos0, m, N_c, k, row_cap(N_c, k), out, out_b_stride);
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
@@ -1029,8 +1056,7 @@ static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_
     const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
     auto ckern = topk_lr_collect_kernel<ST>;
     cudaFuncSetAttribute(ckern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-    ckern<<<rows * p.n_chunks, TOPK_THREADS, csmem, s>>>(scores, ld, n_q_rows, q_pos0, m, N_c, k, p.n_chunks, w,
-                                                        wmax, wmax_ld);
+    (void)launch_pdl(ckern, dim3(rows * p.n_chunks), dim3(TOPK_THREADS), csmem, s, scores, ld, n_q_rows, q_pos0, m, N_c, k, p.n_chunks, w, wmax, wmax_ld);
     return launch_select(scores, ld, n_q_rows, q_pos0, m, N_c, k, w, rows, out, out_b_stride, s);
 }
 
