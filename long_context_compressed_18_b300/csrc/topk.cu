@@ -577,6 +577,68 @@ __device__ void collect_entries(const ST* __restrict__ row, int c0, int len, uin
     }
 }
 
+// collect_entries restricted to the 32-entry runs of the chunk listed in
+// runs[0..nr) (run j covers chunk entries 32 runs[j] .. 32 runs[j] + 31):
+// the runs whose largest key (the indexer's warp maximum) reaches thr, the
+// only ones that can hold an entry with key >= thr.  Eight lanes take a run,
+// four consecutive entries each, and every lane issues its loads for U runs'
+// worth before testing them.
+template <typename ST>
+__device__ void collect_runs(const ST* __restrict__ row, int c0, int len, uint32_t thr, const uint16_t* runs,
+                             int nr, uint32_t* lkey, int32_t* lidx, uint32_t cap, uint32_t* n_loc)
+{
+    const bool take_all = thr == 0u;
+    const float tf = key_value(thr);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const ST* src = row + c0;
+    const bool vec = aligned4(src);
+    constexpr int U = 4;   // run steps a lane loads at once (4 runs a warp a step)
+    for (int j0 = warp * 4 * U; j0 < nr; j0 += TOPK_WARPS * 4 * U) {
+        float v[U][4];
+        int e0[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 4 + (lane >> 3);
+            e0[u] = j < nr ? 32 * (int)runs[j] + 4 * (lane & 7) : len;
+            if (vec && e0[u] + 4 <= len) {
+                const float4 f = ScoreIO<ST>::at4(src, e0[u] >> 2);
+                v[u][0] = f.x; v[u][1] = f.y; v[u][2] = f.z; v[u][3] = f.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[u][q] = e0[u] + q < len ? ScoreIO<ST>::at(src, e0[u] + q) : 0.f;
+            }
+        }
+        uint32_t mask = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (e0[u] + q < len && (take_all || v[u][q] >= tf)) mask |= 1u << (4 * u + q);
+        if (!__any_sync(0xFFFFFFFFu, mask != 0u)) continue;
+        uint32_t incl = __popc(mask);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t wb = 0;
+        if (lane == 31) wb = atomicAdd(n_loc, tot);
+        uint32_t pos = __shfl_sync(0xFFFFFFFFu, wb, 31) + incl - __popc(mask);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (mask >> (4 * u + q) & 1u) {
+                    if (pos < cap) {
+                        lkey[pos] = score_key(v[u][q]);
+                        lidx[pos] = c0 + e0[u] + q;
+                    }
+                    ++pos;
+                }
+    }
+}
+
 // Collection threshold from the row's warp maxima (wmax: the largest score
 // key of each run of 32 consecutive entries, written by the indexer): a key
 // at or below the kk-th largest of the nw = ceil(L / 32) maxima.  Those kk
@@ -648,14 +710,35 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_lr_collect_kernel(
     // storage, which holds them meanwhile), else from the same samples
     static_assert(LR_LOCAL_CAP >= LR_SAMPLES, "sample keys live in the chunk list");
     const int nw = (L + 31) / 32;
-    const uint32_t thr = (wmax && nw <= 2 * LR_LOCAL_CAP)
-                             ? wmax_threshold(wmax + (long long)r * wmax_ld, nw, min(k, L), lkey, sh)
-                             : sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, lkey, sh);
-    __syncthreads();
-    if (threadIdx.x == 0) n_loc_s = 0;
+    const bool by_runs = wmax && nw <= 2 * LR_LOCAL_CAP;
+    const uint32_t thr = by_runs ? wmax_threshold(wmax + (long long)r * wmax_ld, nw, min(k, L), lkey, sh)
+                                 : sample_threshold<LR_SAMPLES>(scores + (long long)r * ld, L, k, lkey, sh);
+    __shared__ uint16_t runs_s[LR_CHUNK / 32];
+    __shared__ uint32_t n_runs_s;
+    if (threadIdx.x == 0) {
+        n_loc_s = 0;
+        n_runs_s = 0;
+    }
     __syncthreads();
     const uint32_t cap = (uint32_t)w.cap;
-    collect_entries(scores + (long long)r * ld, c0, len, thr, lkey, lidx, LR_LOCAL_CAP, &n_loc_s);
+    if (by_runs) {
+        // the chunk's runs whose maximum (still in lkey) reaches thr; whole
+        // warps take part in each ballot
+        const int q0 = c0 / 32, nq = (len + 31) / 32, lane = threadIdx.x & 31;
+        for (int t = threadIdx.x; t < ((nq + 31) & ~31); t += TOPK_THREADS) {
+            const bool hit = t < nq && lkey[q0 + t] >= thr;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, hit);
+            uint32_t p0 = 0;
+            if (lane == 0 && bal) p0 = atomicAdd(&n_runs_s, (uint32_t)__popc(bal));
+            p0 = __shfl_sync(0xFFFFFFFFu, p0, 0);
+            if (hit) runs_s[p0 + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)t;
+        }
+        __syncthreads();
+        collect_runs(scores + (long long)r * ld, c0, len, thr, runs_s, (int)n_runs_s, lkey, lidx, LR_LOCAL_CAP,
+                     &n_loc_s);
+    } else {
+        collect_entries(scores + (long long)r * ld, c0, len, thr, lkey, lidx, LR_LOCAL_CAP, &n_loc_s);
+    }
     __syncthreads();
     const uint32_t n_all = n_loc_s;
     // counts every entry, even past the row's capacity; a chunk that
