@@ -13,6 +13,7 @@
 // rows up to TOPK_MAX_SINGLE take one fused CTA each (sampled threshold,
 // collection, select); longer rows take two kernels (collect with a sampled
 // threshold, select) over many CTAs.
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -97,8 +98,11 @@ __device__ void find_bin(TopkShared& sh, uint32_t rem)
     }
     if (lane == 31) sh.scan[warp] = incl;
     __syncthreads();
-    uint32_t before = incl - tot;
-    for (int w = 0; w < warp; ++w) before += sh.scan[w];
+    // the earlier warps' totals, summed across the lanes
+    uint32_t x = lane < warp ? sh.scan[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    uint32_t before = incl - tot + x;
 #pragma unroll
     for (int q = 0; q < BPT; ++q) {
         if (before < rem && before + c[q] >= rem) {
@@ -656,11 +660,23 @@ __device__ uint32_t wmax_threshold(const uint32_t* __restrict__ wrow, int nw, in
     const int tid = threadIdx.x;
     clear_hist(sh, 2048);
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    for (int x = tid; x < nw; x += TOPK_THREADS) {
-        const uint32_t key = __ldcg(wrow + x);
-        keys[x] = key;
-        lo = min(lo, key);
-        hi = max(hi, key);
+    constexpr int WU = 16;   // loads in flight a thread
+    for (int x0 = 0; x0 < nw; x0 += TOPK_THREADS * WU) {
+        uint32_t v[WU];
+#pragma unroll
+        for (int u = 0; u < WU; ++u) {
+            const int x = x0 + u * TOPK_THREADS + tid;
+            v[u] = x < nw ? __ldcg(wrow + x) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < WU; ++u) {
+            const int x = x0 + u * TOPK_THREADS + tid;
+            if (x < nw) {
+                keys[x] = v[u];
+                lo = min(lo, v[u]);
+                hi = max(hi, v[u]);
+            }
+        }
     }
 #pragma unroll
     for (int dd = 16; dd > 0; dd >>= 1) {
@@ -951,6 +967,164 @@ __device__ void select_streaming(const ST* __restrict__ row, int L, int kk, Topk
                        [&](int pos, int e) { if (pos < kk) o[pos] = e; });
 }
 
+// Words of select_sparse's scratch: the 2,048 bucket starts, then kk slots.
+__host__ __device__ constexpr int sparse_scratch_words(int k) { return 2048 + ((k + 3) & ~3); }
+
+// Exact selection for an entry list much shorter than its row (ekey, eidx: n
+// entries in shared memory, every entry of the row whose key is at least
+// some threshold, n >= kk; L <= 2^20), in steps sized by the list, not by
+// the row:
+//   1. the keys are spread as (key - lo) << s (strictly increasing) and
+//      counted in a 2,048-bin histogram; the bin b holding rank kk is found;
+//   2. the entries of bin b (usually a handful) are ranked among themselves
+//      by direct comparison, which gives the kk-th largest key T exactly;
+//   3. the kk entries with key >= T are counted into 2,048 buckets of
+//      consecutive indices (j >> shift), the bucket starts found by a prefix
+//      sum, and each entry scattered into its bucket; each one's slot is then
+//      its bucket start plus the number of its bucket's entries with a
+//      smaller index, so the output is in ascending index order.
+// Returns false, before writing o, when the list needs the general route
+// (select_entries): bin b holds more entries than the CTA has threads, or
+// only some of the entries equal to T are taken (index order among ties).
+// scratch: sparse_scratch_words(kk) words of shared memory.
+__device__ bool select_sparse(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* scratch,
+                              TopkShared& sh, int32_t* __restrict__ o)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    clear_hist(sh, 2048);
+    if (tid == 0) sh.n_cand = 0;
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        lo = min(lo, ekey[e]);
+        hi = max(hi, ekey[e]);
+    }
+#pragma unroll
+    for (int dd = 16; dd > 0; dd >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
+    }
+    if (lane == 0) {
+        sh.scan[warp] = lo;
+        sh.warp_take[warp] = hi;
+    }
+    __syncthreads();
+    lo = lane < TOPK_WARPS ? sh.scan[lane] : 0xFFFFFFFFu;
+    hi = lane < TOPK_WARPS ? sh.warp_take[lane] : 0u;
+#pragma unroll
+    for (int dd = 16; dd > 0; dd >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
+    }
+    const uint32_t span = hi - lo;
+    const int shl = span ? __clz(span) : 0;
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const uint32_t tk = (ekey[e] - lo) << shl;
+        ekey[e] = tk;
+        atomicAdd(&sh.hist[tk >> 21], 1u);
+    }
+    __syncthreads();
+    // 1. the bin of rank kk; rem = kk's rank within it
+    find_bin<2048>(sh, (uint32_t)kk);
+    const uint32_t b1 = sh.bin, rem = (uint32_t)kk - sh.above;
+    const unsigned lt = (1u << lane) - 1u;
+    if (tid == 0) sh.warp_eq[0] = 0xFFFFFFFFu;   // no T found yet
+    for (int base = 0; base < n; base += TOPK_THREADS) {
+        const int e = base + tid;
+        const uint32_t key = e < n ? ekey[e] : 0u;
+        const bool m = e < n && (key >> 21) == b1;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
+        uint32_t p0 = 0;
+        if (lane == 0 && bal) p0 = atomicAdd(&sh.n_cand, (uint32_t)__popc(bal));
+        p0 = __shfl_sync(0xFFFFFFFFu, p0, 0);
+        if (m) {
+            const uint32_t pos = p0 + __popc(bal & lt);
+            if (pos < CAND_CAP) sh.cand[pos] = key;
+        }
+    }
+    __syncthreads();
+    const int nc = (int)sh.n_cand;
+    if (nc > TOPK_THREADS) return false;
+    // 2. T: the candidate with gt < rem <= gt + eq (every thread holding a
+    // key equal to T writes the same values)
+    if (tid < nc) {
+        const uint32_t kt = sh.cand[tid];
+        uint32_t gt = 0, eq = 0;
+        for (int c = 0; c < nc; ++c) {
+            const uint32_t kc = sh.cand[c];
+            gt += kc > kt;
+            eq += kc == kt;
+        }
+        if (gt < rem && rem <= gt + eq) {
+            sh.bin = kt;
+            sh.above = rem - gt;   // taken among the keys equal to T
+            sh.warp_eq[0] = eq;    // keys equal to T
+        }
+    }
+    __syncthreads();
+    const uint32_t T = sh.bin;
+    if (sh.above != sh.warp_eq[0]) return false;
+    // 3. ascending index order by bucket counting
+    const int bits = L > 1 ? 32 - __clz((uint32_t)(L - 1)) : 1;
+    const int shift = bits > 11 ? bits - 11 : 0;
+    uint32_t* start = scratch;        // [2048]
+    int32_t* slot = reinterpret_cast<int32_t*>(scratch + 2048);   // [kk]
+    __syncthreads();                  // every thread has read sh.bin / sh.above
+    clear_hist(sh, 2048);
+    __syncthreads();
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const int j = eidx[e];
+        if (ekey[e] >= T && (unsigned)j < (unsigned)L) atomicAdd(&sh.hist[j >> shift], 1u);
+    }
+    __syncthreads();
+    {
+        constexpr int BPT = 2048 / TOPK_THREADS;
+        uint32_t c[BPT], tot = 0;
+#pragma unroll
+        for (int q = 0; q < BPT; ++q) {
+            c[q] = sh.hist[tid * BPT + q];
+            tot += c[q];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+            if (lane >= o2) incl += t;
+        }
+        if (lane == 31) sh.scan[warp] = incl;
+        __syncthreads();
+        uint32_t x = lane < warp ? sh.scan[lane] : 0u;
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o2);
+        uint32_t run = x + incl - tot;
+#pragma unroll
+        for (int q = 0; q < BPT; ++q) {
+            start[tid * BPT + q] = run;
+            sh.hist[tid * BPT + q] = run;   // the bucket's fill cursor
+            run += c[q];
+        }
+        if (tid == TOPK_THREADS - 1) sh.n_cand = run;   // entries taken
+    }
+    __syncthreads();
+    if (sh.n_cand != (uint32_t)kk) return false;   // cannot happen for a valid list
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const int j = eidx[e];
+        if (ekey[e] >= T && (unsigned)j < (unsigned)L) {
+            const uint32_t p = atomicAdd(&sh.hist[j >> shift], 1u);
+            if (p < (uint32_t)kk) slot[p] = j;
+        }
+    }
+    __syncthreads();
+    for (int q = tid; q < kk; q += TOPK_THREADS) {
+        const int j = slot[q];
+        const int b = j >> shift;
+        const uint32_t st = start[b], en = min(sh.hist[b], (uint32_t)kk);
+        uint32_t r = 0;
+        for (uint32_t i = st; i < en; ++i) r += slot[i] < j;
+        o[st + r] = j;
+    }
+    return true;
+}
+
 template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc, int k,
@@ -974,8 +1148,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
     const ST* row = scores + (long long)r * ld;
     const uint32_t got = __ldcg(w.cnt + r);
     if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
-        uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem_raw);   // two bitmaps of the row
-        uint32_t* ekey = bitmaps + 2 * bitmap_words(L);               // [cap]
+        // two bitmaps of the row (or select_sparse's scratch), then the list
+        uint32_t* bitmaps = reinterpret_cast<uint32_t*>(smem_raw);
+        uint32_t* ekey = bitmaps + max(2 * bitmap_words(L), sparse_scratch_words(k));   // [cap]
         int32_t* eidx = reinterpret_cast<int32_t*>(ekey + w.cap);
         const int n = (int)got;
         for (int base = 0; base < n; base += TOPK_THREADS * 8) {
@@ -997,7 +1172,10 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
             }
         }
         __syncthreads();
-        select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o);
+        if (!select_sparse(ekey, eidx, n, kk, L, bitmaps, sh, o)) {
+            __syncthreads();
+            select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o);
+        }
         return;
     }
     select_streaming(row, L, kk, sh, o);
@@ -1100,7 +1278,7 @@ static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, Q
                                  int k, const LongRowWs& w, int rows, int32_t* out, long long out_b_stride,
                                  cudaStream_t s)
 {
-    size_t smem = (size_t)2 * bitmap_words(N_c) * 4 + (size_t)w.cap * 8;
+    size_t smem = (size_t)std::max(2 * bitmap_words(N_c), sparse_scratch_words(k)) * 4 + (size_t)w.cap * 8;
     const int fast_ok = smem <= (size_t)200 * 1024;
     if (!fast_ok) smem = 0;
     auto kern = topk_lr_select_kernel<ST>;
