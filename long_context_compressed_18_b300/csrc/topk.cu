@@ -1199,7 +1199,10 @@ static int row_cap(int N_c, int k)
     return 2 * k + 2048 > 4096 ? 2 * k + 2048 : 4096;
 }
 
-static size_t row_smem_bytes(int N_c, int k) { return (size_t)row_cap(N_c, k) * 8 + (size_t)2 * bitmap_words(N_c) * 4; }
+static size_t row_smem_bytes(int N_c, int k)
+{
+    return (size_t)row_cap(N_c, k) * 8 + (size_t)std::max(2 * bitmap_words(N_c), sparse_scratch_words(k)) * 4;
+}
 
 template <typename ST>
 __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
@@ -1233,7 +1236,10 @@ __global__ void __launch_bounds__(TOPK_THREADS, 2) topk_kernel(
     __syncthreads();
     const uint32_t n = n_cnt;
     if (n >= (uint32_t)kk && n <= (uint32_t)cap) {
-        select_entries(ekey, eidx, (int)n, kk, L, bitmaps, sh, o);
+        if (!select_sparse(ekey, eidx, (int)n, kk, L, bitmaps, sh, o)) {
+            __syncthreads();
+            select_entries(ekey, eidx, (int)n, kk, L, bitmaps, sh, o);
+        }
         return;
     }
     select_streaming(row, L, kk, sh, o);
