@@ -75,9 +75,21 @@ __device__ __forceinline__ void compress_store(const float (&acc)[8], int g, int
         uint32_t scc = f32x2_to_e4m3x2(__fdiv_rn(amax, 6.f), 0.f) & 0xFFu;
         if ((scc & 0x7Fu) == 0) scc = 0x01u;
         const float sc = e4m3x2_to_f32x2((uint16_t)scc).x;
+        // x / sc correctly rounded without a division per element: the
+        // correctly rounded reciprocal once, then q0 = |x| (1/sc) corrected
+        // by one FMA residual step (Markstein's final step of FMA-based
+        // division), the sign taken from x (so -0 and negatives that round to
+        // zero keep their sign).  Compared with IEEE division over every fp32
+        // significand of x and every positive E4M3 scale it never differs.
+        const float rcp = __frcp_rn(sc);
         float y[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) y[c] = __fdiv_rn(acc[c], sc);
+        for (int c = 0; c < 8; ++c) {
+            const float ax = fabsf(acc[c]);
+            const float q0 = __fmul_rn(ax, rcp);
+            const float res = __fmaf_rn(-q0, sc, ax);
+            y[c] = copysignf(__fmaf_rn(res, rcp, q0), acc[c]);
+        }
         const uint32_t packed = f32x8_to_e2m1x8(y);
         if (live) {
             reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(out) + r * (d / 2))[g] = packed;
