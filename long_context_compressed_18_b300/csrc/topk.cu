@@ -988,17 +988,22 @@ __host__ __device__ constexpr int sparse_scratch_words(int k) { return 2048 + ((
 // Returns false, before writing o, when the list needs the general route
 // (select_entries): bin b holds more entries than the CTA has threads, or
 // only some of the entries equal to T are taken (index order among ties).
-// scratch: sparse_scratch_words(kk) words of shared memory.
+// scratch: sparse_scratch_words(kk) words of shared memory.  lo_t / hi_t:
+// this thread's minimum / maximum over the keys it wrote to ekey, when the
+// caller tracked them (have_range), else the keys are scanned here.
 __device__ bool select_sparse(uint32_t* ekey, const int32_t* eidx, int n, int kk, int L, uint32_t* scratch,
-                              TopkShared& sh, int32_t* __restrict__ o)
+                              TopkShared& sh, int32_t* __restrict__ o, bool have_range = false,
+                              uint32_t lo_t = 0xFFFFFFFFu, uint32_t hi_t = 0u)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     clear_hist(sh, 2048);
     if (tid == 0) sh.n_cand = 0;
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-    for (int e = tid; e < n; e += TOPK_THREADS) {
-        lo = min(lo, ekey[e]);
-        hi = max(hi, ekey[e]);
+    uint32_t lo = lo_t, hi = hi_t;
+    if (!have_range) {
+        for (int e = tid; e < n; e += TOPK_THREADS) {
+            lo = min(lo, ekey[e]);
+            hi = max(hi, ekey[e]);
+        }
     }
 #pragma unroll
     for (int dd = 16; dd > 0; dd >>= 1) {
@@ -1028,18 +1033,13 @@ __device__ bool select_sparse(uint32_t* ekey, const int32_t* eidx, int n, int kk
     // 1. the bin of rank kk; rem = kk's rank within it
     find_bin<2048>(sh, (uint32_t)kk);
     const uint32_t b1 = sh.bin, rem = (uint32_t)kk - sh.above;
-    const unsigned lt = (1u << lane) - 1u;
+    // the bin's entries (their order is irrelevant); usually a handful, so
+    // each one reserves its own slot
     if (tid == 0) sh.warp_eq[0] = 0xFFFFFFFFu;   // no T found yet
-    for (int base = 0; base < n; base += TOPK_THREADS) {
-        const int e = base + tid;
-        const uint32_t key = e < n ? ekey[e] : 0u;
-        const bool m = e < n && (key >> 21) == b1;
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
-        uint32_t p0 = 0;
-        if (lane == 0 && bal) p0 = atomicAdd(&sh.n_cand, (uint32_t)__popc(bal));
-        p0 = __shfl_sync(0xFFFFFFFFu, p0, 0);
-        if (m) {
-            const uint32_t pos = p0 + __popc(bal & lt);
+    for (int e = tid; e < n; e += TOPK_THREADS) {
+        const uint32_t key = ekey[e];
+        if ((key >> 21) == b1) {
+            const uint32_t pos = atomicAdd(&sh.n_cand, 1u);
             if (pos < CAND_CAP) sh.cand[pos] = key;
         }
     }
@@ -1148,6 +1148,17 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
         return;
     }
     const ST* row = scores + (long long)r * ld;
+    // the list's first TOPK_THREADS * 8 slots are loaded together with its
+    // count (slots past the count hold stale words and are dropped; the list
+    // has at least that many slots), saving a round trip
+    static_assert(TOPK_THREADS * 8 <= 8192, "the first batch lies inside the row's list");
+    uint32_t kv[8];
+    int32_t iv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        kv[u] = __ldcg(w.key + (size_t)r * w.cap + u * TOPK_THREADS + tid);
+        iv[u] = __ldcg(w.idx + (size_t)r * w.cap + u * TOPK_THREADS + tid);
+    }
     const uint32_t got = __ldcg(w.cnt + r);
     if (fast_ok && got >= (uint32_t)kk && got <= (uint32_t)w.cap) {
         // two bitmaps of the row (or select_sparse's scratch), then the list
@@ -1155,14 +1166,15 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
         uint32_t* ekey = bitmaps + max(2 * bitmap_words(L), sparse_scratch_words(k));   // [cap]
         int32_t* eidx = reinterpret_cast<int32_t*>(ekey + w.cap);
         const int n = (int)got;
+        uint32_t lo = 0xFFFFFFFFu, hi = 0u;
         for (int base = 0; base < n; base += TOPK_THREADS * 8) {
-            uint32_t kv[8];
-            int32_t iv[8];
+            if (base > 0) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = base + u * TOPK_THREADS + tid;
-                kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : 0u;
-                iv[u] = e < n ? __ldcg(w.idx + (size_t)r * w.cap + e) : 0;
+                for (int u = 0; u < 8; ++u) {
+                    const int e = base + u * TOPK_THREADS + tid;
+                    kv[u] = e < n ? __ldcg(w.key + (size_t)r * w.cap + e) : 0u;
+                    iv[u] = e < n ? __ldcg(w.idx + (size_t)r * w.cap + e) : 0;
+                }
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -1170,11 +1182,13 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_lr_select_kernel(
                 if (e < n) {
                     ekey[e] = kv[u];
                     eidx[e] = iv[u];
+                    lo = min(lo, kv[u]);
+                    hi = max(hi, kv[u]);
                 }
             }
         }
         __syncthreads();
-        if (!select_sparse(ekey, eidx, n, kk, L, bitmaps, sh, o)) {
+        if (!select_sparse(ekey, eidx, n, kk, L, bitmaps, sh, o, true, lo, hi)) {
             __syncthreads();
             select_entries(ekey, eidx, n, kk, L, bitmaps, sh, o);
         }
