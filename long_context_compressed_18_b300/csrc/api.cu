@@ -137,7 +137,8 @@ SplitPlan attn_split_plan(int n_q, long long set_len)
 csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, QPos q_pos0, int m, int N_c, int H_I,
                         int d_I, const void* q_idx, csa_dtype_t q_dtype, const float* q_scale, const void* k_idx,
                         csa_dtype_t k_dtype, const void* k_scale, const float* head_w, bool relu, void* scores,
-                        bool sbf16, void* ws, cudaStream_t s, uint32_t* wmax = nullptr, int wmax_ld = 0)
+                        bool sbf16, void* ws, cudaStream_t s, uint32_t* wmax = nullptr, int wmax_ld = 0,
+                        uint32_t* zero_words = nullptr, int n_zero = 0)
 {
     if (q_dtype == CSA_F32) {
         return cuda_status(launch_indexer_f32(reinterpret_cast<const float*>(q_idx), q_scale, head_w, relu,
@@ -179,7 +180,7 @@ csa_status_t run_scores(int B, int n_q, int i_start, int n_q_rows, QPos q_pos0, 
     if (st != CSA_OK) return st;
     return cuda_status(launch_indexer_tc(fp8, T, tq, tk, q_scale, head_w, relu, ksc, scores, sbf16, B, n_q, i_start,
                                          n_q_rows,
-                                         q_pos0, m, N_c, num_sms(), wmax, wmax_ld, kfp4, s),
+                                         q_pos0, m, N_c, num_sms(), wmax, wmax_ld, kfp4, s, zero_words, n_zero),
                        "indexer_tc launch");
 }
 
@@ -623,14 +624,16 @@ static csa_status_t index_topk_impl(int B, int n_q, int64_t q_pos0, const int64_
     for (int i0 = 0; i0 < n_q; i0 += rows) {
         const int nr = std::min(rows, n_q - i0);
         if (N_c > 0 && fused_index_topk(q_dtype, nr, N_c, k)) {
-            // scores plus the rows' warp maxima in one kernel, then the top-k
-            // with its collection threshold taken from them
+            // scores plus the rows' warp maxima in one kernel, which also
+            // clears the top-k's row counters, then the top-k with its
+            // collection threshold taken from the maxima
             const int ld = topk_wmax_ld(N_c);
             st = run_scores(B, n_q, i0, nr, qp, m, N_c, H_I, d_I, q_idx, q_dtype, q_scale, k_idx, k_dtype, k_scale,
-                            head_weight, relu != 0, scores, sbf16, w_scores_ws, s, w_wmax, ld);
+                            head_weight, relu != 0, scores, sbf16, w_scores_ws, s, w_wmax, ld,
+                            topk_row_counters(w_topk), B * nr);
             if (st != CSA_OK) return st;
             st = cuda_status(launch_topk(scores, sbf16, N_c, B, nr, qp.shifted(i0), m, N_c, k, topk + (size_t)i0 * k, n_q,
-                                         w_topk, s, w_wmax, ld),
+                                         w_topk, s, w_wmax, ld, true),
                              "topk launch");
             if (st != CSA_OK) return st;
             continue;

@@ -187,9 +187,13 @@ __global__ void __launch_bounds__(idx::threads<T, KFP4>(), KFP4 ? 2 : 1) indexer
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const float* __restrict__ q_scale, const float* __restrict__ head_w, int relu, const float* __restrict__ k_scale,
     void* __restrict__ scores, int score_bf16, int n_q_total, int i_start, int n_q_rows, QPos qp, int m,
-    int Nc, int n_splits, int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld)
+    int Nc, int n_splits, int split_tiles, uint32_t* __restrict__ wmax, int wmax_ld,
+    uint32_t* __restrict__ zero_words, int n_zero)
 {
     grid_dep_entry();
+    // words the next kernel expects cleared (the top-k's row counters)
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int x = threadIdx.x; x < n_zero; x += blockDim.x) zero_words[x] = 0u;
     using C = idx::Cfg<FP8, T, KFP4>;
     static_assert(!WMAX || T == 1, "warp maxima: decode groups");
     extern __shared__ uint8_t smem_raw[];
@@ -588,7 +592,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
                              bool relu, const float* k_scale, void* scores, bool score_bf16, int B, int n_q_total,
                              int i_start,
                              int n_q_rows, QPos q_pos0, int m, int Nc, int num_sms, uint32_t* wmax,
-                             int wmax_ld, cudaStream_t s)
+                             int wmax_ld, cudaStream_t s, uint32_t* zero_words = nullptr, int n_zero = 0)
 {
     using C = idx::Cfg<FP8, T, KFP4>;
     const int n_groups = (n_q_rows + T - 1) / T;
@@ -606,7 +610,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     auto kern = indexer_tc_kernel<FP8, T, WMAX, KFP4>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     dim3 grid(n_groups * splits, B);
-    (void)launch_pdl(kern, dim3(grid), dim3(idx::threads<T, KFP4>()), C::SMEM, s, tq, tk, q_scale, head_w, relu ? 1 : 0, k_scale, scores, score_bf16 ? 1 : 0, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld);
+    (void)launch_pdl(kern, dim3(grid), dim3(idx::threads<T, KFP4>()), C::SMEM, s, tq, tk, q_scale, head_w, relu ? 1 : 0, k_scale, scores, score_bf16 ? 1 : 0, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, splits, split_tiles, wmax, wmax_ld, zero_words, n_zero);
     return cudaGetLastError();
 }
 
@@ -614,17 +618,18 @@ cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUte
                               const float* q_scale, const float* head_w, bool relu, const float* k_scale,
                               void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, QPos q_pos0, int m, int Nc,
-                              int num_sms, uint32_t* wmax, int wmax_ld, bool kfp4, cudaStream_t s)
+                              int num_sms, uint32_t* wmax, int wmax_ld, bool kfp4, cudaStream_t s,
+                              uint32_t* zero_words, int n_zero)
 {
     if (kfp4) {   // packed E2M1 keys widened in the kernel: E4M3 queries, decode groups
         if (!fp8 || T != 1) return cudaErrorInvalidValue;
-        if (wmax) return launch_tc<true, 1, true, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        if (wmax) return launch_tc<true, 1, true, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s, zero_words, n_zero);
         return launch_tc<true, 1, false, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);
     }
     if (wmax) {   // decode groups (T = 1) only
         if (T != 1) return cudaErrorInvalidValue;
-        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
-        return launch_tc<false, 1, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s);
+        if (fp8) return launch_tc<true, 1, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s, zero_words, n_zero);
+        return launch_tc<false, 1, true>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, wmax, wmax_ld, s, zero_words, n_zero);
     }
     if (fp8) {
         if (T == 4) return launch_tc<true, 4, false>(tq, tk, q_scale, head_w, relu, k_scale, scores, score_bf16, B, n_q_total, i_start, n_q_rows, q_pos0, m, Nc, num_sms, nullptr, 0, s);

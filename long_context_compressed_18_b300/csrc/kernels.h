@@ -86,9 +86,15 @@ size_t topk_workspace_bytes(long long rows, int N_c, int k);
 // row), written by the decode indexer; the collection then takes its
 // threshold from them instead of from a sample of the row.
 // scores: fp32, or bf16 when scores_bf16 (selection on the stored values).
+// counters_clear: the rows' counters (topk_row_counters) were cleared by the
+// kernel before (the fused route's indexer), so no memset is issued.
 cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, QPos q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
-                        cudaStream_t s, const uint32_t* wmax = nullptr, int wmax_ld = 0);
+                        cudaStream_t s, const uint32_t* wmax = nullptr, int wmax_ld = 0,
+                        bool counters_clear = false);
+// The long-row route's per-row counters (one word a row, at the start of the
+// top-k workspace), which every long-row selection needs cleared first.
+uint32_t* topk_row_counters(void* ws);
 bool topk_long_rows(int N_c, int k);
 int topk_wmax_ld(int N_c);
 size_t topk_wmax_bytes(long long rows, int N_c);
@@ -106,7 +112,8 @@ cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUte
                               const float* q_scale, const float* head_w, bool relu, const float* k_scale,
                               void* scores, bool score_bf16, int B,
                               int n_q_total, int i_start, int n_q_rows, QPos q_pos0, int m, int Nc,
-                              int num_sms, uint32_t* wmax, int wmax_ld, bool kfp4, cudaStream_t s);
+                              int num_sms, uint32_t* wmax, int wmax_ld, bool kfp4, cudaStream_t s,
+                              uint32_t* zero_words = nullptr, int n_zero = 0);
 cudaError_t launch_indexer_f32(const float* q, const float* q_scale, const float* head_w, bool relu,
                                const float* k, const float* k_scale, void* scores, bool score_bf16, int B,
                                int n_q_total, int i_start, int n_q_rows,

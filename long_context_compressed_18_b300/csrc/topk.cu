@@ -1312,7 +1312,7 @@ static cudaError_t launch_select(const ST* scores, long long ld, int n_q_rows, Q
 template <typename ST>
 static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_rows, QPos q_pos0, int m,
                                  int N_c, int k, int32_t* out, long long out_b_stride, void* ws, cudaStream_t s,
-                                 const uint32_t* wmax, int wmax_ld)
+                                 const uint32_t* wmax, int wmax_ld, bool counters_clear)
 {
     const long long rows_ll = (long long)B * n_q_rows;
     if (rows_ll == 0) return cudaSuccess;
@@ -1334,8 +1334,10 @@ static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_
         return cudaGetLastError();
     }
     const LongRowWs w = lr_ws(ws, rows, k);
-    cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)rows * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
+    if (!counters_clear) {
+        cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)rows * sizeof(uint32_t), s);
+        if (e != cudaSuccess) return e;
+    }
     const size_t csmem = (size_t)LR_LOCAL_CAP * 8;
     auto ckern = topk_lr_collect_kernel<ST>;
     cudaFuncSetAttribute(ckern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
@@ -1345,14 +1347,16 @@ static cudaError_t launch_topk_t(const ST* scores, long long ld, int B, int n_q_
 
 cudaError_t launch_topk(const void* scores, bool scores_bf16, long long ld, int B, int n_q_rows, QPos q_pos0,
                         int m, int N_c, int k, int32_t* out, long long out_b_stride, void* ws,
-                        cudaStream_t s, const uint32_t* wmax, int wmax_ld)
+                        cudaStream_t s, const uint32_t* wmax, int wmax_ld, bool counters_clear)
 {
     if (scores_bf16)
         return launch_topk_t(reinterpret_cast<const __nv_bfloat16*>(scores), ld, B, n_q_rows, q_pos0, m, N_c, k, out,
-                             out_b_stride, ws, s, wmax, wmax_ld);
+                             out_b_stride, ws, s, wmax, wmax_ld, counters_clear);
     return launch_topk_t(reinterpret_cast<const float*>(scores), ld, B, n_q_rows, q_pos0, m, N_c, k, out,
-                         out_b_stride, ws, s, wmax, wmax_ld);
+                         out_b_stride, ws, s, wmax, wmax_ld, counters_clear);
 }
+
+uint32_t* topk_row_counters(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 bool topk_long_rows(int N_c, int k) { return topk_plan(N_c, k).n_chunks > 1; }
 
