@@ -267,14 +267,18 @@ __global__ void __launch_bounds__(idx::threads<T, KFP4>(), KFP4 ? 2 : 1) indexer
             for (int a = 0; a < C::ATOMS; ++a)
                 tma_load_2d(sQ + a * C::Q_ATOM, &tmap_q, bar_q, a * (idx::ATOM_BYTES_ROW / C::ELEM), qrow);
             int issued = 0;
+            // decode groups read each key tile once: mark its lines first for
+            // eviction, so the stream leaves the scores (which the top-k reads
+            // next) in L2
+            const uint64_t kpol = l2_policy_evict_first();
             if constexpr (KFP4) {
                 // packed tiles into the raw ring; the converter warps free its stages
                 for (int li = 0; li < n_tiles; ++li) {
                     const int rs = li % C::RAW_STAGES;
                     if (!mbar_wait(&bar_raw_empty[rs], ((li / C::RAW_STAGES) & 1) ^ 1, abort_flag)) break;
                     mbar_arrive_expect_tx(&bar_raw_full[rs], C::RAW_BYTES);
-                    tma_load_2d(sRaw + rs * C::RAW_BYTES, &tmap_k, &bar_raw_full[rs], 0,
-                                b * Nc + (tile0 + li) * idx::BLOCK_KEYS);
+                    tma_load_2d_hint(sRaw + rs * C::RAW_BYTES, &tmap_k, &bar_raw_full[rs], 0,
+                                     b * Nc + (tile0 + li) * idx::BLOCK_KEYS, kpol);
                     issued = li + 1;
                 }
             } else {
@@ -285,8 +289,13 @@ __global__ void __launch_bounds__(idx::threads<T, KFP4>(), KFP4 ? 2 : 1) indexer
                     mbar_arrive_expect_tx(&bar_full[st], C::K_BYTES);
                     const int krow = b * Nc + (tile0 + li) * idx::BLOCK_KEYS;
                     uint8_t* dst = sK + st * C::K_BYTES;
-                    for (int a = 0; a < C::ATOMS; ++a)
-                        tma_load_2d(dst + a * C::K_ATOM, &tmap_k, &bar_full[st], a * (idx::ATOM_BYTES_ROW / C::ELEM), krow);
+                    for (int a = 0; a < C::ATOMS; ++a) {
+                        if constexpr (T == 1)
+                            tma_load_2d_hint(dst + a * C::K_ATOM, &tmap_k, &bar_full[st],
+                                             a * (idx::ATOM_BYTES_ROW / C::ELEM), krow, kpol);
+                        else
+                            tma_load_2d(dst + a * C::K_ATOM, &tmap_k, &bar_full[st], a * (idx::ATOM_BYTES_ROW / C::ELEM), krow);
+                    }
                     issued = li + 1;
                 }
             }
