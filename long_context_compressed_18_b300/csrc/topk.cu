@@ -457,11 +457,12 @@ __device__ uint32_t sample_threshold(const ST* __restrict__ row, int L, int kk, 
         sh.warp_take[warp] = hi;
     }
     __syncthreads();
-    lo = 0xFFFFFFFFu;
-    hi = 0u;
-    for (int q = 0; q < TOPK_WARPS; ++q) {
-        lo = min(lo, sh.scan[q]);
-        hi = max(hi, sh.warp_take[q]);
+    lo = lane < TOPK_WARPS ? sh.scan[lane] : 0xFFFFFFFFu;
+    hi = lane < TOPK_WARPS ? sh.warp_take[lane] : 0u;
+#pragma unroll
+    for (int dd = 16; dd > 0; dd >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
+        hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
     }
     const uint32_t span = hi - lo;
     const int shl = span ? __clz(span) : 0;
