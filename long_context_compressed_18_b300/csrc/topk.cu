@@ -408,15 +408,26 @@ __device__ __forceinline__ void stream_keys(const ST* __restrict__ row, int c0, 
     }
 }
 
+// The float whose key is k (inverse of score_key on keys of non-NaN values).
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Collection threshold of a row: the keys of S = min(L, smax) entries in
 // runs of 32 consecutive entries (whole cache lines), evenly spaced, ranked at
 // t = 2 * kk * S / L + 8 (twice the expected rank of the k-th largest key,
 // plus a margin).  The threshold only has to lie at or below the sample key
-// of rank t: the samples' keys are spread as (key - lo) << s, s putting the
-// top bit of hi - lo at bit 31, two histogram levels (bits 31..21, then 20..10
-// within the selected bin) locate rank t, and the lowest key whose spread key
-// falls in that second-level bin is returned.  keys: shared buffer of smax
-// entries.
+// of rank t.  When the samples' values span a finite, non-zero range, one
+// 2,048-bin histogram linear in the value (a monotone map, so a higher bin
+// never holds a smaller value) locates the bin holding rank t, and the
+// smallest sample key in that bin is returned.  (Bins of the key are
+// logarithmic in the value: across a sign change one is a quarter octave,
+// far too coarse on its own.)  Otherwise the keys are spread as
+// (key - lo) << s, s putting the top bit of hi - lo at bit 31, two histogram
+// levels (bits 31..21, then 20..10 within the selected bin) locate rank t,
+// and the lowest key whose spread key falls in that second-level bin is
+// returned.  keys: shared buffer of smax entries.
 template <int SMAX, typename ST>
 __device__ uint32_t sample_threshold(const ST* __restrict__ row, int L, int kk, uint32_t* keys, TopkShared& sh)
 {
@@ -464,12 +475,32 @@ __device__ uint32_t sample_threshold(const ST* __restrict__ row, int L, int kk, 
         lo = min(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, dd));
         hi = max(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, dd));
     }
+    const long long want = 2ll * kk * S / L + 8;
+    const int t_rank = (int)(want < S ? want : S);
+    const float vlo = key_value(lo), vspan = key_value(hi) - vlo, vscale = 2048.f / vspan;
+    if (isfinite(vspan) && vspan > 0.f && isfinite(vscale)) {
+        auto vbin = [&](float x) { return min(2047, (int)((x - vlo) * vscale)); };
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (u * TOPK_THREADS + tid < S) atomicAdd(&sh.hist[vbin(v[u])], 1u);
+        if (tid == 0) sh.n_cand = 0xFFFFFFFFu;   // the bin's smallest key
+        __syncthreads();
+        find_bin<2048>(sh, (uint32_t)t_rank);
+        const int vb = (int)sh.bin;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = u * TOPK_THREADS + tid;
+            if (q < S && vbin(v[u]) == vb) atomicMin(&sh.n_cand, keys[q]);
+        }
+        __syncthreads();
+        const uint32_t T = sh.n_cand;
+        __syncthreads();
+        return T;
+    }
     const uint32_t span = hi - lo;
     const int shl = span ? __clz(span) : 0;
     for (int q = tid; q < S; q += TOPK_THREADS) atomicAdd(&sh.hist[((keys[q] - lo) << shl) >> 21], 1u);
     __syncthreads();
-    const long long want = 2ll * kk * S / L + 8;
-    const int t_rank = (int)(want < S ? want : S);
     find_bin<2048>(sh, (uint32_t)t_rank);
     const uint32_t b1 = sh.bin, rem = (uint32_t)t_rank - sh.above;
     // second level: bits 20..10 of the spread keys in that bin
@@ -488,11 +519,6 @@ __device__ uint32_t sample_threshold(const ST* __restrict__ row, int L, int kk, 
     return T;
 }
 
-// The float whose key is k (inverse of score_key on keys of non-NaN values).
-__device__ __forceinline__ float key_value(uint32_t k)
-{
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
 
 // Appends every entry e of [c0, c0 + len) of a row with key >= thr to the
 // shared list (lkey, lidx) of capacity cap through the shared counter *n_loc;
