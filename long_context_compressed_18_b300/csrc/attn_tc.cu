@@ -50,6 +50,8 @@
 // Split key sets (decode-shaped calls) write unnormalised partials (o, m, l)
 // that attn_combine_kernel merges in split order, so results stay
 // deterministic and independent of the batch size.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -73,13 +75,17 @@ constexpr int D = 128;                    // head dim
 constexpr int ATOM = 128 * 128;           // 128 rows x 128 bytes (64 bf16 columns)
 constexpr int K_BYTES = 2 * ATOM;
 constexpr int V_BYTES = 2 * ATOM;
-constexpr int TMEM_COLS = 512;
-constexpr int S_COL = 0;                  // S buffers at columns 0 and 128
-constexpr int O_COL = 256;                // O accumulator at columns 256..383
+constexpr int S_COL = 0;                  // S buffers at columns 0 (and 128)
+// SBUFS S buffers (1 or 2), then the O accumulator; the allocation is the
+// next power of two (two S buffers: 512 columns, one CTA an SM; one S
+// buffer: 256 columns, so two CTAs share an SM's tensor memory)
+constexpr int o_col(int sbufs) { return sbufs * KT; }
+constexpr int tmem_cols(int sbufs) { return sbufs == 1 ? 256 : 512; }
 constexpr uint32_t IDESC_S = instr_desc(1u, 1u, ROWS, KT);          // bf16, both K-major
 constexpr uint32_t IDESC_PV = instr_desc(1u, 1u, ROWS, D, 0u, 1u);  // B (= V) MN-major
 constexpr uint32_t FULL = 0xFFFFFFFFu;
 constexpr int MAX_LIST = 4096;            // selected entries one CTA stages (sparse mode)
+constexpr int SMALL_MAX_TILES = 8;        // dense key sets of at most this many tiles: the small configuration
 
 // QROWS: Q rows loaded per CTA.  With 64 (one token of 64 heads) the two
 // 64-column Q blocks sit 8 KB apart; the MMA still reads 128 rows, and rows
@@ -95,8 +101,11 @@ template <int MODE, int STAGES, int QROWS> struct Cfg {
 };
 }  // namespace atc
 
-template <int MODE, int STAGES, int QROWS>
-__global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
+// SBUFS = 1 (dense modes, one ring stage): the small configuration for short
+// key sets, two CTAs an SM -- S_j is issued only after P_{j-1} V_{j-1} has
+// completed, and one CTA's set-up and loads overlap the other's work.
+template <int MODE, int STAGES, int QROWS, int SBUFS>
+__global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, SBUFS == 1 ? 2 : 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
     const __grid_constant__ CUtensorMap tmap_v, const AttnTcParams p)
 {
@@ -104,6 +113,9 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
     using namespace atc;
     using C = Cfg<MODE, STAGES, QROWS>;
     using R = Roles<MODE>;
+    static_assert(SBUFS == 2 || (SBUFS == 1 && !R::SPARSE), "one S buffer: dense modes");
+    constexpr int O_COL = o_col(SBUFS);
+    constexpr int TMEM_COLS = tmem_cols(SBUFS);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = base;
@@ -324,9 +336,9 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
         if (lane == 0 && n_tiles > 0) {
             const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
             auto issue_pv = [&](int i) -> bool {
-                const int st = i % STAGES, sb = i & 1;
+                const int st = i % STAGES, sb = i % SBUFS;
                 if (!mbar_wait(&v_full[st], (i / STAGES) & 1, abort_flag)) return false;
-                if (!mbar_wait(&p_full[sb], (i >> 1) & 1, abort_flag)) return false;
+                if (!mbar_wait(&p_full[sb], (i / SBUFS) & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t a = tmem + S_COL + sb * KT;
 #pragma unroll
@@ -342,10 +354,12 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
             };
             bool ok = mbar_wait(bar_q, 0, abort_flag);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j % STAGES, sb = j & 1;
+                const int st = j % STAGES, sb = j % SBUFS;
+                // the one S buffer holds P_{j-1}: issue P_{j-1} V_{j-1} first
+                if (SBUFS == 1 && j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
                 if (!mbar_wait(&k_full[st], (j / STAGES) & 1, abort_flag)) { ok = false; break; }
-                // S buffer sb still holds P_{j-2} until P_{j-2} V_{j-2} has completed
-                if (j >= 2 && !mbar_wait(o_full, (j - 2) & 1, abort_flag)) { ok = false; break; }
+                // S buffer sb still holds P_{j - SBUFS} until P_{j - SBUFS} V_{j - SBUFS} has completed
+                if (j >= SBUFS && !mbar_wait(o_full, (j - SBUFS) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + S_COL + sb * KT;
 #pragma unroll
@@ -358,7 +372,7 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
                 }
                 umma_commit(&s_full[sb]);
                 umma_commit(&k_empty[st]);
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                if (SBUFS == 2 && j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
             if (ok) issue_pv(n_tiles - 1);
             umma_commit(bar_mma_done);      // all MMAs of this CTA retired
@@ -401,8 +415,8 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
         bool ok = true;
         if (MODE == 0 && n_tiles > 0) ok = __all_sync(FULL, mbar_wait(bar_list, 0, abort_flag));
         for (int j = 0; ok && j < n_tiles; ++j) {
-            const int sb = j & 1;
-            const bool w = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag);
+            const int sb = j % SBUFS;
+            const bool w = mbar_wait(&s_full[sb], (j / SBUFS) & 1, abort_flag);
             if (!__all_sync(FULL, w)) { ok = false; break; }
             tc_fence_after();
             if (!warp_idle) {
@@ -454,11 +468,13 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
                     m_ref = m_new;
                     return true;
                 };
-                if constexpr (R::SPARSE) {
+                if constexpr (R::SPARSE || SBUFS == 1) {
                     // two passes over 32-column chunks of S: the row maximum,
                     // then the exponentials (a chunk's P overwrites S columns
-                    // already read: P of chunk q lands in columns 16q .. 16q+15)
-                    const bool all_full = __all_sync(FULL, row_ok && (mk[0] & mk[1] & mk[2] & mk[3]) == FULL);
+                    // already read: P of chunk q lands in columns 16q .. 16q+15);
+                    // the register budget of a 512-thread CTA or of two CTAs an SM
+                    const bool all_full = R::SPARSE ? __all_sync(FULL, row_ok && (mk[0] & mk[1] & mk[2] & mk[3]) == FULL)
+                                                    : __all_sync(FULL, lo_c == 0 && hi_c == KT);
                     auto load_chunk = [&](int q, float (&v)[32]) {
                         tmem_ld32(s_addr + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                         tmem_ld_wait();
@@ -466,7 +482,9 @@ __global__ void __launch_bounds__(atc::Roles<MODE>::THREADS, 1) attn_tc_kernel(
 #pragma unroll
                             for (int u = 0; u < 32; ++u) {
                                 const int c = 32 * q + u;
-                                v[u] = ((mk[c & 3] >> (c >> 2)) & 1u) ? v[u] : -INFINITY;
+                                const bool valid = R::SPARSE ? ((mk[c & 3] >> (c >> 2)) & 1u) != 0u
+                                                             : (unsigned)(c - lo_c) < (unsigned)(hi_c - lo_c);
+                                v[u] = valid ? v[u] : -INFINITY;
                             }
                         }
                     };
@@ -613,11 +631,11 @@ int attn_tc_tokens_per_cta(int mode, int H) { return mode == 0 ? 1 : atc::ROWS /
 
 int attn_tc_q_box_rows(int mode, int H) { return (mode == 0 && H == 64) ? 64 : 128; }
 
-template <int MODE, int STAGES, int QROWS>
+template <int MODE, int STAGES, int QROWS, int SBUFS = 2>
 static void launch_one(dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const AttnTcParams& p, cudaStream_t s)
 {
-    auto kern = attn_tc_kernel<MODE, STAGES, QROWS>;
+    auto kern = attn_tc_kernel<MODE, STAGES, QROWS, SBUFS>;
     constexpr int smem = atc::Cfg<MODE, STAGES, QROWS>::SMEM;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     (void)launch_pdl(kern, dim3(grid), dim3(atc::Roles<MODE>::THREADS), smem, s, tq, tk, tv, p);
@@ -632,10 +650,19 @@ cudaError_t launch_attn_tc(int mode, const CUtensorMap& tq, const CUtensorMap& t
     if (mode == 0) {
         if (p.H == 64) launch_one<0, 3, 64>(grid, tq, tk, tv, p, s);
         else launch_one<0, 2, 128>(grid, tq, tk, tv, p, s);
-    } else if (mode == 1) {
-        launch_one<1, 3, 128>(grid, tq, tk, tv, p, s);
     } else {
-        launch_one<2, 3, 128>(grid, tq, tk, tv, p, s);
+        // dense modes: short key sets (the stack's SWA windows and HCA prefixes)
+        // take the small configuration, two CTAs an SM
+        long long set_max = mode == 2 ? p.window + p.T - 1 : std::min<long long>(p.N_kv, (p.q_pos0 + p.n_q) / p.m);
+        if (p.n_splits > 1) set_max = std::min<long long>(set_max, p.split_len);
+        const bool small = (set_max + atc::KT - 1) / atc::KT <= atc::SMALL_MAX_TILES;
+        if (mode == 1) {
+            if (small) launch_one<1, 1, 128, 1>(grid, tq, tk, tv, p, s);
+            else launch_one<1, 3, 128>(grid, tq, tk, tv, p, s);
+        } else {
+            if (small) launch_one<2, 1, 128, 1>(grid, tq, tk, tv, p, s);
+            else launch_one<2, 3, 128>(grid, tq, tk, tv, p, s);
+        }
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.n_splits == 1) return e;
