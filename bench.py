@@ -218,9 +218,10 @@ def run_decode(args, torch, dist, rank, world):
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
-        # Lightning Indexer + top-k in one call (the indexer kernel collects
-        # each row's candidates; a select kernel finishes the selection), then
-        # sparse attention
+        # Lightning Indexer + top-k in one call (the indexer writes the scores
+        # and each row's 32-entry maxima; a collection kernel keeps the runs
+        # that reach the threshold the maxima give, a select kernel finishes),
+        # then sparse attention (key slices + their combine)
         if ev:
             ev[0].record(stream)
         lib.csa_index_topk(B, 1, s.q_pos0, s.m, Nc, HI, dI, k, x["idx_q"], lib.E4M3, x["idx_q_scale"],
@@ -393,10 +394,11 @@ def run_decode(args, torch, dist, rank, world):
         cpu = {"value": nq / tt, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{nq} of the 32 decode queries (full 262,144-entry caches), {tt:.1f} s"}
 
-    # library kernels: the collecting indexer and the select (after a memset
-    # of the row counters that is not one of them); attention (+ the slice
-    # combine when the key set is split)
-    launches_per_step = 2 + (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
+    # library kernels a step: the indexer (which also writes the warp maxima
+    # and clears the row counters), the collection and the select of the
+    # long-row top-k (rows over 32,768 entries; else one top-k kernel), then
+    # attention (+ the slice combine when the key set is split)
+    launches_per_step = (3 if Nc > 32768 else 2) + (2 if lib.csa_sparse_attn_workspace_size(B, 1, H, d, k) else 1)
     res = {
         "metric": METRIC, "value": _job_rate(world, B * K, ms), "unit": "queries/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -408,8 +410,8 @@ def run_decode(args, torch, dist, rank, world):
                    "index_scores": args.scores, "top_k": k,
                    "attention": f"{H}x{d} bf16",
                    "l2": f"inputs ({in_gb:.1f} GB per GPU) exceed L2; no flush",
-                   "launch": "one step (indexer with fused top-k collection, select, sparse attention) captured "
-                             "in a CUDA graph and replayed",
+                   "launch": "one step (indexer with warp maxima, top-k collect and select, sparse attention "
+                             "and slice combine) captured in a CUDA graph and replayed",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * K,
