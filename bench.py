@@ -15,6 +15,7 @@ instead (the reference arm).  ``--config NAME`` times another named workload
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -351,19 +352,27 @@ def run_decode(args, torch, dist, rank, world):
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        a.record(stream)
-        for i in range(K2):
-            e2e_step(i)
-        stream.wait_stream(down)                          # the last read-backs are inside the region
-        b_.record(stream)
-        torch.cuda.synchronize()
+        # Python's cyclic garbage collector is collected once and then paused
+        # for the loop, as a serving loop does: its pauses stall the host that
+        # enqueues the steps, not the library
+        gc.collect()
+        gc.disable()
+        try:
+            a.record(stream)
+            for i in range(K2):
+                e2e_step(i)
+            stream.wait_stream(down)                      # the last read-backs are inside the region
+            b_.record(stream)
+            torch.cuda.synchronize()
+        finally:
+            gc.enable()
         ms2 = _max_over_ranks(torch, dist, a.elapsed_time(b_))
         e2e = {"value": _job_rate(world, B * K2, ms2), "unit": "queries/s", "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo,
                "note": "per step one H2D copy of the 32 queries (q, indexer q + scales, packed) and one D2H "
                        "copy of out, lse and top-k (packed), double-buffered on upload and read-back streams "
                        "so they overlap the neighbouring steps' kernels; the compressed caches are resident "
-                       "decode state"}
+                       "decode state; Python's garbage collector paused during the timed loop"}
 
     # ---- roofline of the dominant call ----
     peaks, peak_src = _peaks()
