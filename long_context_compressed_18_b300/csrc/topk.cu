@@ -1,18 +1,20 @@
 // Top-k selection ("DeepSeek V4 技术解读" §2.1: the Lightning Indexer keeps the
 // k highest-scoring compressed entries per query).
 //
-// Exact radix select on order-preserving 32-bit keys of the fp32 scores
-// (-0 folded onto +0): the k-th largest key T is found with three histogram
-// levels (11, 11 and 10 bits; see radix_threshold), and the selection is
-// every key > T plus the first (k - #{key > T}) elements equal to T in index
-// order -- i.e. ranking by (score desc, index asc) -- written in ascending
-// index order.  No floating-point atomics; the result does not depend on
-// thread scheduling.
+// Exact selection on order-preserving 32-bit keys of the fp32 scores (-0
+// folded onto +0): the k-th largest key T is found exactly (histogram levels
+// over the keys, see radix_threshold, or one spread level plus a direct
+// ranking of the boundary bin, see select_sparse), and the selection is every
+// key > T plus the first (k - #{key > T}) elements equal to T in index order
+// -- i.e. ranking by (score desc, index asc) -- written in ascending index
+// order.  No floating-point atomics; the result does not depend on thread
+// scheduling.
 //
 // Rows up to 16,384 entries take one CTA each with all keys in shared memory;
 // rows up to TOPK_MAX_SINGLE take one fused CTA each (sampled threshold,
-// collection, select); longer rows take two kernels (collect with a sampled
-// threshold, select) over many CTAs.
+// collection, select); longer rows take two kernels (collect, select) over
+// many CTAs, with the collection threshold from a sample of the row or, on
+// the fused decode route, from the indexer's 32-entry maxima.
 #include <algorithm>
 #include <climits>
 
@@ -306,24 +308,27 @@ __global__ void __launch_bounds__(TOPK_THREADS, 3) topk_smem_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Long rows (more than one CTA's capacity): the row counters are cleared, then
-// two kernels.
-//   collect  one CTA per 32768-entry chunk: from keys of 4096 evenly spaced
-//            entries of the row, every chunk CTA derives the same collection
-//            threshold thr -- a key at or below their key of rank
-//            ~2k * 4096 / L (plus a margin), expected to sit well below the
-//            k-th largest key -- then appends every entry of its chunk with
-//            key >= thr to a shared-memory list (4096 entries), whose slice
-//            of the row's entry list is reserved with one global atomic;
+// Long rows (more than one CTA's capacity): the row counters are cleared (a
+// memset, or the fused route's indexer), then two kernels.
+//   collect  one CTA per 32768-entry chunk: every chunk CTA of a row derives
+//            the same collection threshold thr -- from the keys of 4096
+//            evenly spaced entries (a key at or below their key of rank
+//            ~2k * 4096 / L plus a margin), or from the row's 32-entry maxima
+//            written by the indexer (at or below the k-th largest maximum),
+//            so expected to sit below the row's k-th largest key -- then
+//            appends every entry of its chunk with key >= thr (with maxima:
+//            reading only the 32-entry runs whose maximum reaches thr) to a
+//            shared-memory list (4096 entries), whose slice of the row's
+//            entry list is reserved with one global atomic;
 //   select   one CTA per row: if the row collected at least k entries (so
 //            the k-th largest key T is >= thr and every entry with key >= T
-//            was collected) and no more than the list holds, the exact
-//            threshold among the entries is found with the radix levels and
-//            the selected indices -- equal keys taken in index order -- are
-//            marked in a shared-memory bitmap and written in ascending
-//            order.  Otherwise (heavy ties, or a sample that misjudged the
-//            row) the row is selected by the same radix levels and ordered
-//            compaction streaming the row from global memory.
+//            was collected) and no more than the list holds, T is found
+//            exactly among the entries and the selected indices -- equal keys
+//            taken in index order -- are written in ascending order
+//            (select_sparse, or the bitmap route of select_entries for heavy
+//            ties).  Otherwise (a threshold that misjudged the row) the row
+//            is selected by the radix levels and ordered compaction streaming
+//            the row from global memory.
 // Both routes give the exact result; only their speed depends on the data.
 // ---------------------------------------------------------------------------
 constexpr int LR_CHUNK = 32768;
