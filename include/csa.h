@@ -190,7 +190,8 @@ csa_status_t csa_topk_select_noalloc(int B, int n_q, int64_t q_pos0, int m, int 
  * 32,768 entries (decode), the tensor-core indexer also writes the largest
  * score of every 32 consecutive entries, and the selection takes its
  * collection threshold from them (the k-th largest has at least k entries at
- * or above it) instead of from a sample of the row.
+ * or above it) instead of from a sample of the row, and reads only the runs
+ * of 32 whose largest score reaches it.
  * ------------------------------------------------------------------------- */
 size_t csa_index_topk_workspace_size(int B, int n_q, int N_c, int H_I, int d_I, int k,
                                      csa_dtype_t k_dtype, csa_dtype_t score_dtype);

@@ -108,6 +108,8 @@ int indexer_box_rows(int T);
 // scores: fp32, or bf16 (nearest even) when score_bf16.
 // head_w ([B, n_q, H_I] or null) and relu: the weighted / ReLU variant,
 // s = sk * sum_h w_h sq_h max(<q_h, k>, 0).
+// zero_words (n_zero words, or null): cleared by the kernel's first CTA for
+// the kernel that follows (the fused route's top-k row counters).
 cudaError_t launch_indexer_tc(bool fp8, int T, const CUtensorMap& tq, const CUtensorMap& tk,
                               const float* q_scale, const float* head_w, bool relu, const float* k_scale,
                               void* scores, bool score_bf16, int B,
