@@ -168,8 +168,9 @@ __device__ void radix_threshold(const uint32_t* keys, int len, int kk, TopkShare
 
 // Loads len fp32 scores into shared memory as keys and accumulates the
 // first-level histogram.  Each thread keeps four 16-byte loads in flight
-// (a whole 8,192-entry row in one batch), which keeps the kernel within the
-// registers of three CTAs an SM.
+// (a whole 8,192-entry row in one batch), which keeps the kernel near the
+// 32 registers of four CTAs an SM (a few spilled words cost less than the
+// fourth CTA gains).
 template <typename ST>
 __device__ void load_score_keys(const ST* __restrict__ src, int len, uint32_t* keys, TopkShared& sh)
 {
@@ -275,7 +276,7 @@ __device__ void ordered_compact(const uint32_t* keys, int len, uint32_t T, int t
 // in shared memory, one radix select over them and an ordered compaction;
 // writes the final indices, -1 padded.
 template <typename ST>
-__global__ void __launch_bounds__(TOPK_THREADS, 3) topk_smem_kernel(
+__global__ void __launch_bounds__(TOPK_THREADS, 4) topk_smem_kernel(
     const ST* __restrict__ scores, long long ld, int n_q_rows, QPos qp, int m, int Nc,
     int k, int32_t* __restrict__ out, long long out_b_stride)
 {
