@@ -615,8 +615,11 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const CUtensorMap& tk, const
     // waves of CTAs: 12 for E4M3 keys (a sweep of 3-16 at batch 32: 12 best,
     // 0.2015 -> 0.1935 ms for index + top-k), 4 for the widening E2M1 route
     // (12 there: 0.278 -> 0.296 ms)
+    // (12 waves only while a CTA keeps at least 16 key tiles: small batches
+    // would otherwise spend more on per-CTA set-up than they gain)
     const long long target = (long long)num_sms * per_sm * (KFP4 ? 4 : 12);
     int splits = (int)std::min<long long>(tiles, std::max<long long>(1, (target + (long long)B * n_groups - 1) / ((long long)B * n_groups)));
+    if (!KFP4) splits = std::max(1, std::min(splits, tiles / 16));
     const int split_tiles = (tiles + splits - 1) / splits;
     splits = (tiles + split_tiles - 1) / split_tiles;
     auto kern = indexer_tc_kernel<FP8, T, WMAX, KFP4>;
